@@ -1,0 +1,357 @@
+"""Seeded synthetic inputs for the H3 DiT block, shared by the CPU oracle and the CUDA path.
+
+Nothing here computes the block: this module only draws reproducible tensors (weights,
+activations, timestep embeddings), lays out the packed sequence ``[text | conditions |
+audio | video]`` with its per-row modality tags, timestep indices and (t, h, w) rotary
+positions, and quantises bf16 master weights into the weight-only INT8 group-32 storage
+format.  Every array is produced on the host from (seed, stream) so that a parity test can
+hand the same bytes to both sides.
+
+Pages followed for the input shapes:
+- packed sequence and per-row modality tag: minimax-h3-mlx README, "Architecture";
+- block geometry (hidden 5376, 56x128 heads, SwiGLU 14336): same section, component table;
+- 40-units-per-second shared rotary clock: minimax-h3-mlx README, "Validation";
+- video/audio sigma shifts 12.0 / 3.0 and 77 distinct timesteps: minimax-h3-mlx README,
+  "AdaLN precompute";
+- weight-only INT8 with group size 32 ("a8g32"): mlx-h3 README, "Local model layout".
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gen.c")
+_LIB_PATH = os.path.join(_HERE, "libh3synth.so")
+_lib = None
+
+TAG_TEXT, TAG_AUDIO, TAG_VIDEO = 0, 1, 2
+
+
+def build_lib(force: bool = False) -> str:
+    """Compile the generator (plain C, gcc) next to its source; returns the .so path."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build_lib())
+        u64, f64, i32, vp = ctypes.c_uint64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p
+        for name in ("h3s_normal_bf16", "h3s_normal_f32", "h3s_normal_f64"):
+            fn = getattr(lib, name)
+            fn.argtypes = [u64, u64, u64, f64, f64, vp, i32]
+            fn.restype = None
+        lib.h3s_raw_u64.argtypes = [u64, u64, u64, vp]
+        lib.h3s_raw_u64.restype = None
+        _lib = lib
+    return _lib
+
+
+def _threads() -> int:
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+def raw_u64(seed: int, stream: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint64)
+    _load().h3s_raw_u64(seed, stream, n, out.ctypes.data)
+    return out
+
+
+def normal_bf16(seed: int, stream: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    """N(mean, std^2) samples rounded to bfloat16, returned as raw uint16 bit patterns."""
+    out = np.empty(shape, dtype=np.uint16)
+    _load().h3s_normal_bf16(seed, stream, out.size, mean, std, out.ctypes.data, _threads())
+    return out
+
+
+def normal_f32(seed: int, stream: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    out = np.empty(shape, dtype=np.float32)
+    _load().h3s_normal_f32(seed, stream, out.size, mean, std, out.ctypes.data, _threads())
+    return out
+
+
+def normal_f64(seed: int, stream: int, shape, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    out = np.empty(shape, dtype=np.float64)
+    _load().h3s_normal_f64(seed, stream, out.size, mean, std, out.ctypes.data, _threads())
+    return out
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen raw bfloat16 bit patterns to float32 (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (nearest, ties to even) and return the bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (u + (np.uint32(0x7FFF) + ((u >> 16) & np.uint32(1)))) >> 16
+    nan = (u & 0x7F800000) == 0x7F800000
+    nan &= (u & 0x007FFFFF) != 0
+    r = np.where(nan, (u >> 16) | 0x40, r)
+    return r.astype(np.uint16)
+
+
+# --------------------------------------------------------------------------------------
+# configurations
+# --------------------------------------------------------------------------------------
+
+
+@dataclass(frozen=True)
+class Dims:
+    """Block geometry: hidden H, heads x head_dim, SwiGLU width F, timestep-embedding width Dt."""
+
+    hidden: int
+    heads: int
+    head_dim: int
+    ffn: int
+    temb_dim: int
+    n_tags: int = 3
+    rope_theta: float = 10000.0
+    ln_eps: float = 1e-6
+    qk_eps: float = 1e-6
+
+    @property
+    def inner(self) -> int:
+        return self.heads * self.head_dim
+
+    @property
+    def rope_sections(self) -> tuple:
+        """Frequency pairs given to the (t, h, w) axes: hd/8, 3hd/16, 3hd/16."""
+        hd = self.head_dim
+        return (hd // 8, 3 * hd // 16, 3 * hd // 16)
+
+
+TINY = Dims(hidden=192, heads=4, head_dim=64, ffn=512, temb_dim=96)
+H3 = Dims(hidden=5376, heads=56, head_dim=128, ffn=14336, temb_dim=2688)
+
+
+@dataclass(frozen=True)
+class Layout:
+    """Segment sizes of the packed sequence; video is frames x height x width latent tokens."""
+
+    text: int
+    cond: tuple  # (h, w) grid of one condition image, or () for none
+    audio: int
+    video: tuple  # (frames, h, w)
+
+    @property
+    def n_cond(self) -> int:
+        return int(np.prod(self.cond)) if self.cond else 0
+
+    @property
+    def n_video(self) -> int:
+        return int(np.prod(self.video))
+
+    @property
+    def n_rows(self) -> int:
+        return self.text + self.n_cond + self.audio + self.n_video
+
+
+@dataclass(frozen=True)
+class Config:
+    name: str
+    dims: Dims
+    layout: Layout
+    seed: int
+    n_blocks: int = 1
+    n_timesteps: int = 1
+    int8: bool = False
+    timesteps: tuple = field(default=(500.0,))
+
+
+def _schedule_timesteps(steps: int = 40, video_shift: float = 12.0, audio_shift: float = 3.0, keep: int = 77):
+    """Distinct timestep values of a shifted rectified-flow run.
+
+    Sigmas are the first `steps` points of an even grid from 1 to 0; each schedule applies the
+    shift sigma' = s*sigma / (1 + (s-1)*sigma) (the exponential shift with mu = ln s); the
+    timestep is 1000*sigma'.  The union of both schedules is sorted descending and the first
+    `keep` values are kept, so the table has exactly the 77 rows of a 40-step run.
+    Returns (values, video_index_per_step, audio_index_per_step).
+    """
+    sig = np.linspace(1.0, 0.0, steps + 1)[:steps]
+
+    def shift(s, x):
+        return s * x / (1.0 + (s - 1.0) * x)
+
+    tv = np.round(1000.0 * shift(video_shift, sig), 6)
+    ta = np.round(1000.0 * shift(audio_shift, sig), 6)
+    allv = sorted(set(tv.tolist()) | set(ta.tolist()), reverse=True)[:keep]
+    idx = {v: i for i, v in enumerate(allv)}
+    vi = [idx.get(v, len(allv) - 1) for v in tv]
+    ai = [idx.get(v, len(allv) - 1) for v in ta]
+    return tuple(allv), vi, ai
+
+
+_T77, _VIDX, _AIDX = _schedule_timesteps()
+
+CONFIGS = {
+    "tiny": Config("tiny", TINY, Layout(16, (), 24, (2, 4, 4)), seed=0, timesteps=(0.5,)),
+    "block1829": Config("block1829", H3, Layout(256, (), 37, (6, 16, 16)), seed=1),
+    "block12936": Config("block12936", H3, Layout(256, (), 200, (32, 15, 26)), seed=2),
+    "block12936_int8": Config("block12936_int8", H3, Layout(256, (), 200, (32, 15, 26)), seed=3, int8=True),
+    "trunk33720": Config(
+        "trunk33720", H3, Layout(256, (24, 42), 200, (32, 24, 42)), seed=4, n_blocks=50, n_timesteps=77,
+        timesteps=_T77,
+    ),
+}
+
+
+# --------------------------------------------------------------------------------------
+# packed sequence
+# --------------------------------------------------------------------------------------
+
+
+def packed_rows(cfg: Config, step: int = 0):
+    """Per-row modality tag (u8), timestep index (i32) and rotary position (f32 [N, 3]).
+
+    Rows are packed [text | conditions | audio | video].  Positions share one clock of 40
+    units per second: text p = 0..L-1 as (p, p, p); origin O = L; the condition image sits at
+    t = O with its (h, w) grid; audio row i at t = O + i as (t, t, t); video latent frame f at
+    t = O + f * 40*4/24 (4x temporal compression at 24 fps) with grid (h, w).  Condition rows
+    carry the video tag.  Text, condition and video rows take the video schedule's timestep
+    for `step`, audio rows the audio schedule's.
+    """
+    lay = cfg.layout
+    n = lay.n_rows
+    tag = np.empty(n, np.uint8)
+    tidx = np.zeros(n, np.int32)
+    pos = np.zeros((n, 3), np.float32)
+    r = 0
+    L = lay.text
+    p = np.arange(L, dtype=np.float64)
+    tag[r:r + L] = TAG_TEXT
+    pos[r:r + L] = np.stack([p, p, p], 1)
+    r += L
+    origin = float(L)
+    if lay.cond:
+        ch, cw = lay.cond
+        hh, ww = np.meshgrid(np.arange(ch), np.arange(cw), indexing="ij")
+        nc = ch * cw
+        tag[r:r + nc] = TAG_VIDEO
+        pos[r:r + nc, 0] = origin
+        pos[r:r + nc, 1] = hh.reshape(-1)
+        pos[r:r + nc, 2] = ww.reshape(-1)
+        r += nc
+    A = lay.audio
+    ta = origin + np.arange(A, dtype=np.float64)
+    tag[r:r + A] = TAG_AUDIO
+    pos[r:r + A] = np.stack([ta, ta, ta], 1)
+    audio_rows = slice(r, r + A)
+    r += A
+    F, Hh, Ww = lay.video
+    ff, hh, ww = np.meshgrid(np.arange(F), np.arange(Hh), np.arange(Ww), indexing="ij")
+    nv = F * Hh * Ww
+    tag[r:r + nv] = TAG_VIDEO
+    pos[r:r + nv, 0] = origin + ff.reshape(-1) * (40.0 * 4.0 / 24.0)
+    pos[r:r + nv, 1] = hh.reshape(-1)
+    pos[r:r + nv, 2] = ww.reshape(-1)
+    r += nv
+    assert r == n
+    if cfg.n_timesteps > 1:
+        tidx[:] = _VIDX[step % len(_VIDX)]
+        tidx[audio_rows] = _AIDX[step % len(_AIDX)]
+    return tag, tidx, pos
+
+
+def sinusoidal_temb(t_values, dim: int) -> np.ndarray:
+    """Timestep embedding [cos(t*w_k) | sin(t*w_k)], w_k = exp(-ln(1e4) * k / (dim/2)), float32."""
+    t = np.asarray(t_values, dtype=np.float64).reshape(-1, 1)
+    half = dim // 2
+    w = np.exp(-math.log(1e4) * np.arange(half, dtype=np.float64) / half)
+    ang = t * w[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+# --------------------------------------------------------------------------------------
+# tensors
+# --------------------------------------------------------------------------------------
+
+# stream ids: (block << 8) | tensor
+_T_X, _T_WQKV, _T_BQKV, _T_WO, _T_BO, _T_W1, _T_B1, _T_W2, _T_B2, _T_QN, _T_KN, _T_AW, _T_AB = range(1, 14)
+
+
+def _stream(block: int, tensor: int) -> int:
+    return (block << 8) | tensor
+
+
+def activations(cfg: Config) -> np.ndarray:
+    """x ~ N(0, 1), bf16 bits [N, H]."""
+    return normal_bf16(cfg.seed, _stream(0xFFFF, _T_X), (cfg.layout.n_rows, cfg.dims.hidden))
+
+
+def block_weights(cfg: Config, block: int = 0, qk_norm: bool = True) -> dict:
+    """One block's linear weights and biases as bf16 bits; N(0, 0.02), QK-norm weights 1 + N(0, 0.02).
+
+    Shapes follow the checkpoint layout: qkv [3I, H] with rows interleaved per head
+    ([h: q, k, v]), o [H, I], fc1 [2F, H] (first F rows = gate), fc2 [H, F].
+    """
+    d = cfg.dims
+    H, I, F, hd = d.hidden, d.inner, d.ffn, d.head_dim
+    s = cfg.seed
+    w = {
+        "wqkv": normal_bf16(s, _stream(block, _T_WQKV), (3 * I, H), 0.0, 0.02),
+        "bqkv": normal_bf16(s, _stream(block, _T_BQKV), (3 * I,), 0.0, 0.02),
+        "wo": normal_bf16(s, _stream(block, _T_WO), (H, I), 0.0, 0.02),
+        "bo": normal_bf16(s, _stream(block, _T_BO), (H,), 0.0, 0.02),
+        "w1": normal_bf16(s, _stream(block, _T_W1), (2 * F, H), 0.0, 0.02),
+        "b1": normal_bf16(s, _stream(block, _T_B1), (2 * F,), 0.0, 0.02),
+        "w2": normal_bf16(s, _stream(block, _T_W2), (H, F), 0.0, 0.02),
+        "b2": normal_bf16(s, _stream(block, _T_B2), (H,), 0.0, 0.02),
+    }
+    if qk_norm:
+        w["qnorm"] = normal_bf16(s, _stream(block, _T_QN), (hd,), 1.0, 0.02)
+        w["knorm"] = normal_bf16(s, _stream(block, _T_KN), (hd,), 1.0, 0.02)
+    return w
+
+
+def adaln_weights(cfg: Config, block: int = 0) -> tuple:
+    """adaln_proj of one block: W [18H, Dt] and b [18H], bf16 bits, N(0, 0.02)."""
+    d = cfg.dims
+    s = cfg.seed
+    W = normal_bf16(s, _stream(block, _T_AW), (18 * d.hidden, d.temb_dim), 0.0, 0.02)
+    b = normal_bf16(s, _stream(block, _T_AB), (18 * d.hidden,), 0.0, 0.02)
+    return W, b
+
+
+def temb(cfg: Config) -> np.ndarray:
+    return sinusoidal_temb(cfg.timesteps[: cfg.n_timesteps], cfg.dims.temb_dim)
+
+
+# --------------------------------------------------------------------------------------
+# weight-only INT8 group-32 storage (input recipe for the quantised configuration)
+# --------------------------------------------------------------------------------------
+
+
+def quantize_int8_g32(w_bits: np.ndarray):
+    """Affine 8-bit quantisation of bf16 masters [Nout, K] in groups of 32 along K.
+
+    Per group: lo, hi = min, max; scale = bf16((hi - lo) / 255); qbias = bf16(lo);
+    q = clamp(round_half_even((w - qbias) / scale), 0, 255) in float32 (q = 0 when scale is 0).
+    Returns (q u8 [Nout, K], scale bf16 bits [Nout, K/32], qbias bf16 bits [Nout, K/32]).
+    """
+    w = bf16_bits_to_f32(w_bits)
+    n, k = w.shape
+    assert k % 32 == 0
+    g = w.reshape(n, k // 32, 32)
+    lo = g.min(axis=2)
+    hi = g.max(axis=2)
+    scale_bits = f32_to_bf16_bits((hi - lo) / np.float32(255.0))
+    qb_bits = f32_to_bf16_bits(lo)
+    scale = bf16_bits_to_f32(scale_bits)
+    qb = bf16_bits_to_f32(qb_bits)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = (g - qb[:, :, None]) / scale[:, :, None]
+    t = np.where(scale[:, :, None] == 0, 0.0, t).astype(np.float32)
+    q = np.clip(np.rint(t), 0, 255).astype(np.uint8)
+    return q.reshape(n, k), scale_bits, qb_bits

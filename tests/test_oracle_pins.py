@@ -1,0 +1,404 @@
+"""Pins of the CPU oracle to facts outside itself: closed forms, hand-worked values,
+brute force on tiny inputs, invariants, and figures printed on the pages.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a swapped
+modulation tensor, a wrong RoPE pairing or frequency, a transposed weight) fails it.
+"""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle.h3_oracle as O
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _page(name):
+    with open(os.path.join(GOLDEN, "page_figures.json")) as f:
+        return json.load(f)[name]
+
+
+# ------------------------------------------------------------------------ bf16 rounding
+
+
+def test_round_bf16_known_values():
+    # 1 + 2^-8 is exactly half-way between bf16 neighbours 1 and 1 + 2^-7: ties to even -> 1
+    assert O.round_bf16(1.0 + 2 ** -8) == 1.0
+    # 1 + 3*2^-8 is half-way between 1 + 2^-7 (odd mantissa) and 1 + 2^-6: ties to even -> 1 + 2^-6
+    assert O.round_bf16(1.0 + 3 * 2 ** -8) == 1.0 + 2 ** -6
+    assert O.round_bf16(1.0 + 2 ** -8 + 2 ** -20) == 1.0 + 2 ** -7
+    assert O.round_bf16(-3.0) == -3.0
+    assert O.round_bf16(0.1) == 0.10009765625  # 0x3DCD
+    b = O.to_bf16_bits(np.array([1.0, -2.0, 0.5]))
+    assert list(b) == [0x3F80, 0xC000, 0x3F00]
+
+
+# ------------------------------------------------------------------------ LayerNorm + modulate
+
+
+def test_layernorm_worked_example():
+    x = np.array([[1.0, 2.0, 3.0, 4.0]])
+    # mean 2.5, biased variance 1.25
+    expect = np.array([-1.5, -0.5, 0.5, 1.5]) / math.sqrt(1.25)
+    np.testing.assert_allclose(O.layernorm(x, 0.0)[0], expect, rtol=0, atol=1e-15)
+    shift = np.full((1, 4), 0.1)
+    scale = np.full((1, 4), 1.0)
+    np.testing.assert_allclose(O.adaln_modulate(x, shift, scale, 0.0)[0], 2 * expect + 0.1, atol=1e-15)
+
+
+def test_layernorm_zero_modulation_gives_unit_rows():
+    rng = np.random.default_rng(0)
+    x = rng.normal(3.0, 2.0, size=(5, 64))
+    eps = 1e-6
+    y = O.adaln_modulate(x, np.zeros_like(x), np.zeros_like(x), eps)
+    var = x.var(axis=1)
+    np.testing.assert_allclose(y.mean(axis=1), 0.0, atol=1e-13)
+    np.testing.assert_allclose(y.var(axis=1), var / (var + eps), rtol=1e-12)
+
+
+def test_modulate_is_affine_in_scale_and_shift():
+    rng = np.random.default_rng(1)
+    x = rng.normal(size=(3, 16))
+    n = O.layernorm(x, 1e-6)
+    sc = rng.normal(size=(3, 16))
+    sh = rng.normal(size=(3, 16))
+    y = O.adaln_modulate(x, sh, sc, 1e-6)
+    # scale = -1 annihilates the normalised input, leaving only the shift
+    np.testing.assert_allclose(O.adaln_modulate(x, sh, -np.ones_like(x), 1e-6), sh, atol=1e-15)
+    np.testing.assert_allclose(y - sh, n * (1 + sc), atol=1e-13)
+
+
+# ------------------------------------------------------------------------ table + gather
+
+
+def test_modcache_equals_exact_live_projection():
+    """The table entry equals the live adaln projection of the row's timestep embedding,
+    here evaluated with an exactly rounded sum (math.fsum) on a separate code path."""
+    cfg = synth.CONFIGS["tiny"]
+    te = synth.sinusoidal_temb([0.5, 700.0], cfg.dims.temb_dim)
+    W, b = synth.adaln_weights(cfg, 0)
+    W2, b2 = synth.adaln_weights(cfg, 1)
+    t64, tbf = O.modcache(te, [W, W2], [b, b2])
+    assert t64.shape == (2, 2, 18 * 192)
+    Wf = [synth.bf16_bits_to_f32(W).astype(float), synth.bf16_bits_to_f32(W2).astype(float)]
+    bf = [synth.bf16_bits_to_f32(b).astype(float), synth.bf16_bits_to_f32(b2).astype(float)]
+    rng = np.random.default_rng(2)
+    for t, blk in itertools.product(range(2), range(2)):
+        for j in rng.choice(18 * 192, 40, replace=False):
+            terms = [Wf[blk][j, kk] * float(te[t, kk]) for kk in range(cfg.dims.temb_dim)] + [bf[blk][j]]
+            exact = math.fsum(terms)
+            assert abs(t64[t, blk, j] - exact) <= 1e-15 * max(1.0, abs(exact)) * 8
+            assert tbf[t, blk, j] == O.round_bf16(exact)
+
+
+def test_table_size_matches_pages():
+    shp = _page("adaln_proj_shape")["value"]
+    B, n_out, dt = shp
+    assert n_out == 18 * 5376 and dt == 2688
+    assert round(B * n_out * dt / 1e9, 2) == _page("adaln_params_billion")["value"]
+    assert round(B * n_out * dt * 2 / 1e9, 1) == _page("adaln_resident_gb")["value"]
+    for key in ("cache_mb_40_step_run", "cache_mb_15s_run"):
+        g = _page(key)
+        mb = O.table_bytes(g["timesteps"], g["blocks"], g["hidden"]) / 1e6
+        assert round(mb) == g["value"], (key, mb)
+
+
+def test_gather_selects_tag_and_timestep():
+    H, T = 8, 3
+    # code every entry by (t, j, c) so a wrong index shows up as a wrong code
+    tb = np.zeros((T, 18 * H))
+    for t in range(T):
+        for j in range(18):
+            tb[t, j * H:(j + 1) * H] = 1000 * t + 10 * j + np.arange(H) / 100
+    tag = np.array([0, 1, 2, 2, 1])
+    tidx = np.array([2, 0, 1, 0, 2])
+    for m in range(6):
+        g = O.modulation(tb, tag, tidx, m, H)
+        for r in range(5):
+            j = 6 * tag[r] + m
+            assert np.all(g[r] == 1000 * tidx[r] + 10 * j + np.arange(H) / 100)
+
+
+# ------------------------------------------------------------------------ QK-norm + RoPE
+
+
+def test_rms_norm_closed_form():
+    x = np.array([[[3.0, 4.0]]])  # mean square 12.5
+    y = O.rms_norm(x, np.array([1.0, 2.0]), 0.0)
+    np.testing.assert_allclose(y[0, 0], [3 / math.sqrt(12.5), 8 / math.sqrt(12.5)], atol=1e-15)
+
+
+def _unit(hd, i):
+    x = np.zeros((1, 1, hd))
+    x[0, 0, i] = 1.0
+    return x
+
+
+def test_rope_hand_worked_hd16():
+    """hd = 16: 8 pairs (i, i+8), sections (t, h, w) = (2, 3, 3) pairs, omega_i = 1e4^(-2i/16)."""
+    hd, th, sec = 16, 1e4, (2, 3, 3)
+    assert synth.Dims(16, 1, 16, 16, 16).rope_sections == sec
+    # pair 0 on the t axis, omega 1, pos t = 1: e_0 -> (cos 1) e_0 + (sin 1) e_8
+    y = O.rope(_unit(hd, 0), np.array([[1.0, 0, 0]]), hd, th, sec)[0, 0]
+    assert y[0] == pytest.approx(math.cos(1.0), abs=1e-15) and y[8] == pytest.approx(math.sin(1.0), abs=1e-15)
+    assert np.count_nonzero(np.abs(y) > 1e-15) == 2
+    # pair 1 on the t axis, omega = 10^-0.5, pos t = 2
+    y = O.rope(_unit(hd, 1), np.array([[2.0, 0, 0]]), hd, th, sec)[0, 0]
+    a = 2.0 * 10 ** -0.5
+    assert y[1] == pytest.approx(math.cos(a), abs=1e-15) and y[9] == pytest.approx(math.sin(a), abs=1e-15)
+    # pair 2 is the first h-axis pair, omega = 0.1; the second half of a pair rotates as (-sin, cos)
+    y = O.rope(_unit(hd, 10), np.array([[5.0, 3.0, 7.0]]), hd, th, sec)[0, 0]
+    assert y[2] == pytest.approx(-math.sin(0.3), abs=1e-15) and y[10] == pytest.approx(math.cos(0.3), abs=1e-15)
+    # pair 5 is the first w-axis pair, omega = 10^-2.5
+    y = O.rope(_unit(hd, 5), np.array([[9.0, 9.0, 1.0]]), hd, th, sec)[0, 0]
+    a = 10 ** -2.5
+    assert y[5] == pytest.approx(math.cos(a), abs=1e-15) and y[13] == pytest.approx(math.sin(a), abs=1e-15)
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(3)
+    hd, th = 64, 1e4
+    sec = synth.TINY.rope_sections
+    q = rng.normal(size=(6, 2, hd))
+    k = rng.normal(size=(6, 2, hd))
+    # integer positions so that the shifted positions stay exact in float32
+    pos = rng.integers(0, 50, size=(6, 3)).astype(np.float32)
+    rq = O.rope(q, pos, hd, th, sec)
+    # pair norms preserved
+    half = hd // 2
+    np.testing.assert_allclose(rq[..., :half] ** 2 + rq[..., half:] ** 2, q[..., :half] ** 2 + q[..., half:] ** 2,
+                               rtol=1e-12)
+    # zero position is the identity
+    np.testing.assert_allclose(O.rope(q, np.zeros((6, 3), np.float32), hd, th, sec), q, atol=0)
+    # scores depend on relative position only: shifting every row by one offset per axis
+    shift = np.array([7.0, -3.0, 11.0], np.float32)
+    rk = O.rope(k, pos, hd, th, sec)
+    s0 = np.einsum("nhd,mhd->hnm", rq, rk)
+    rq2 = O.rope(q, pos + shift, hd, th, sec)
+    rk2 = O.rope(k, pos + shift, hd, th, sec)
+    s1 = np.einsum("nhd,mhd->hnm", rq2, rk2)
+    np.testing.assert_allclose(s1, s0, rtol=1e-9, atol=1e-9)
+    # shifting only the keys changes the scores (the rotation is not a no-op)
+    rk3 = O.rope(k, pos + shift, hd, th, sec)
+    assert np.abs(np.einsum("nhd,mhd->hnm", rq, rk3) - s0).max() > 1e-3
+
+
+def test_rope_1d_rows_are_textbook_rope():
+    """(p, p, p) rows: every pair rotates by p * omega_i, as a complex multiplication."""
+    hd = 64
+    rng = np.random.default_rng(4)
+    x = rng.normal(size=(5, 1, hd))
+    p = np.arange(5, dtype=np.float32) * 3.0
+    y = O.rope(x, np.stack([p, p, p], 1), hd, 1e4, synth.TINY.rope_sections)
+    half = hd // 2
+    z = x[:, 0, :half] + 1j * x[:, 0, half:]
+    for r in range(5):
+        for i in range(half):
+            ang = float(p[r]) * 1e4 ** (-2 * i / hd)
+            w = z[r, i] * complex(math.cos(ang), math.sin(ang))
+            assert y[r, 0, i] == pytest.approx(w.real, abs=1e-12)
+            assert y[r, 0, half + i] == pytest.approx(w.imag, abs=1e-12)
+
+
+def test_split_qkv_interleaved_rows():
+    heads, hd = 3, 2
+    y = np.arange(heads * 3 * hd, dtype=float)[None, :]
+    q, k, v = O.split_qkv(y, heads, hd)
+    # head h occupies columns [h*3hd, (h+1)*3hd) as q | k | v
+    assert q[0].tolist() == [[0, 1], [6, 7], [12, 13]]
+    assert k[0].tolist() == [[2, 3], [8, 9], [14, 15]]
+    assert v[0].tolist() == [[4, 5], [10, 11], [16, 17]]
+
+
+# ------------------------------------------------------------------------ attention
+
+
+def _brute_attention(q, k, v):
+    """Pure-Python softmax attention with exactly rounded sums (tiny inputs only)."""
+    n, nh, hd = q.shape
+    out = np.zeros_like(q)
+    for h in range(nh):
+        for r in range(n):
+            s = [math.fsum(q[r, h, d] * k[j, h, d] for d in range(hd)) / math.sqrt(hd) for j in range(n)]
+            m = max(s)
+            e = [math.exp(a - m) for a in s]
+            z = math.fsum(e)
+            for d in range(hd):
+                out[r, h, d] = math.fsum(e[j] * v[j, h, d] for j in range(n)) / z
+    return out
+
+
+@pytest.mark.parametrize("n", [1, 2, 5, 16])
+def test_attention_brute_force(n):
+    rng = np.random.default_rng(10 + n)
+    q, k, v = (rng.normal(size=(n, 2, 4)) * 2 for _ in range(3))
+    np.testing.assert_allclose(O.attention(q, k, v), _brute_attention(q, k, v), rtol=1e-12, atol=1e-13)
+
+
+def test_attention_invariants():
+    rng = np.random.default_rng(5)
+    n, nh, hd = 12, 2, 8
+    q, k, v = (rng.normal(size=(n, nh, hd)) for _ in range(3))
+    o = O.attention(q, k, v)
+    perm = rng.permutation(n)
+    np.testing.assert_allclose(O.attention(q, k[perm], v[perm]), o, rtol=1e-12, atol=1e-14)
+    # identical keys: uniform weights, output = mean of values
+    kk = np.broadcast_to(k[:1], k.shape)
+    np.testing.assert_allclose(O.attention(q, kk, v), np.broadcast_to(v.mean(0), o.shape), atol=1e-14)
+    # one dominant key selects its value
+    k2 = k.copy() * 0
+    k2[3] = q[0] * 1e3
+    np.testing.assert_allclose(O.attention(q[:1], k2, v)[0], v[3], atol=1e-12)
+    # query subset equals the same rows of the full result
+    np.testing.assert_allclose(O.attention(q, k, v, rows=[4, 0, 7]), o[[4, 0, 7]], atol=0)
+
+
+# ------------------------------------------------------------------------ linears / SwiGLU
+
+
+def test_linear_orientation_and_identity():
+    x = np.array([[1.0, 2.0, 3.0]])
+    w = np.array([[1.0, 0, 0], [0, 0, 1.0]])  # [out=2, in=3]
+    assert O.linear(x, w, np.array([10.0, 20.0])).tolist() == [[11.0, 23.0]]
+    rng = np.random.default_rng(6)
+    xx = rng.normal(size=(4, 7))
+    np.testing.assert_array_equal(O.linear(xx, np.eye(7)), xx)
+
+
+def test_swiglu_closed_form():
+    y = np.array([[0.0, 1.0, -30.0, 5.0, 2.0, 3.0]])  # F = 3: gates [0, 1, -30], values [5, 2, 3]
+    h = O.swiglu(y, 3)[0]
+    assert h[0] == 0.0
+    assert h[1] == pytest.approx(2.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+    assert abs(h[2]) < 1e-11
+    # silu(x) -> x for large x
+    assert O.silu(np.array([40.0]))[0] == pytest.approx(40.0, rel=1e-15)
+
+
+# ------------------------------------------------------------------------ INT8 group 32
+
+
+def test_int8_roundtrip_bound_and_grid_points():
+    cfg = synth.CONFIGS["tiny"]
+    w = synth.block_weights(cfg)["wo"]  # [192, 256]
+    q, sc, qb = synth.quantize_int8_g32(w)
+    wd = O.dequant_int8_g32(q, sc, qb)
+    wm = O.widen_bf16(w)
+    s = np.repeat(O.widen_bf16(sc), 32, axis=1)
+    ulp = np.abs(wd) * 2.0 ** -8  # >= half a bf16 ulp of w'
+    assert np.all(np.abs(wm - wd) <= s / 2 + ulp + 1e-30)
+    # points on the grid qb + j*scale (exactly representable here) come back as j
+    scale_bits = np.array([[O.to_bf16_bits(2.0 ** -7)]], np.uint16)
+    qb_bits = np.array([[O.to_bf16_bits(-0.5)]], np.uint16)
+    j = np.arange(0, 256, 8)[:32]
+    grid = -0.5 + j * 2.0 ** -7
+    gb = O.to_bf16_bits(grid).reshape(1, 32)
+    assert np.all(O.widen_bf16(gb) == grid)
+    q2, s2, b2 = synth.quantize_int8_g32(gb)
+    assert s2[0, 0] == O.to_bf16_bits((grid.max() - grid.min()) / 255)[()]
+    # dequantising the generator's own output of a grid with scale 2^-7 reproduces it
+    qq = j.astype(np.uint8).reshape(1, 32)
+    np.testing.assert_array_equal(O.dequant_int8_g32(qq, scale_bits, qb_bits)[0], grid)
+
+
+def test_int8_constant_group():
+    w = O.to_bf16_bits(np.full((1, 32), 0.25))
+    q, sc, qb = synth.quantize_int8_g32(w)
+    assert np.all(q == 0) and O.widen_bf16(sc)[0, 0] == 0.0
+    assert np.all(O.dequant_int8_g32(q, sc, qb) == 0.25)
+
+
+# ------------------------------------------------------------------------ block structure
+
+
+def _tiny_inputs(seed_block=0):
+    cfg = synth.CONFIGS["tiny"]
+    d = cfg.dims
+    x = synth.activations(cfg)
+    w = synth.block_weights(cfg, seed_block)
+    te = synth.temb(cfg)
+    W, b = synth.adaln_weights(cfg, seed_block)
+    _, tbf = O.modcache(te, [W], [b])
+    tag, tidx, pos = synth.packed_rows(cfg)
+    return cfg, d, x, w, tbf[:, 0, :], tag, tidx, pos
+
+
+def _set_mod(tb, H, m, value, tags=(0, 1, 2)):
+    tb = tb.copy().reshape(tb.shape[0], 18, H)
+    for t in tags:
+        tb[:, 6 * t + m, :] = value
+    return tb.reshape(tb.shape[0], 18 * H)
+
+
+def test_block_zero_gates_is_identity():
+    cfg, d, x, w, tb, tag, tidx, pos = _tiny_inputs()
+    tb0 = _set_mod(_set_mod(tb, d.hidden, O.GATE_MSA, 0.0), d.hidden, O.GATE_MLP, 0.0)
+    out = O.block_forward(x, w, tb0, tag, tidx, pos, d)
+    np.testing.assert_array_equal(out, O.widen_bf16(x))
+
+
+def test_block_branch_wiring():
+    """With gate_mlp = 0 the output is the attention branch alone: it must not move with the
+    MLP-branch shift, and must move with the attention-branch shift.  With gate_msa = 0 the
+    output must not depend on the attention weights."""
+    cfg, d, x, w, tb, tag, tidx, pos = _tiny_inputs()
+    H = d.hidden
+    a = O.block_forward(x, w, _set_mod(tb, H, O.GATE_MLP, 0.0), tag, tidx, pos, d)
+    b = O.block_forward(x, w, _set_mod(_set_mod(tb, H, O.GATE_MLP, 0.0), H, O.SHIFT_MLP, 5.0), tag, tidx, pos, d)
+    np.testing.assert_array_equal(a, b)
+    c = O.block_forward(x, w, _set_mod(_set_mod(tb, H, O.GATE_MLP, 0.0), H, O.SHIFT_MSA, 5.0), tag, tidx, pos, d)
+    assert np.abs(c - a).max() > 1e-3
+    w2 = dict(w)
+    w2["wqkv"] = synth.block_weights(cfg, 7)["wqkv"]
+    e = O.block_forward(x, w, _set_mod(tb, H, O.GATE_MSA, 0.0), tag, tidx, pos, d)
+    f = O.block_forward(x, w2, _set_mod(tb, H, O.GATE_MSA, 0.0), tag, tidx, pos, d)
+    np.testing.assert_array_equal(e, f)
+
+
+def test_block_tag_selects_its_own_modulation():
+    """Rows tagged text read only table entries 0..5: changing the audio/video entries leaves
+    text rows' attention-branch input unchanged."""
+    cfg, d, x, w, tb, tag, tidx, pos = _tiny_inputs()
+    H = d.hidden
+    _, parts = O.block_forward(x, w, tb, tag, tidx, pos, d, return_parts=True)
+    tb2 = _set_mod(tb, H, O.SHIFT_MSA, 3.0, tags=(1, 2))
+    _, parts2 = O.block_forward(x, w, tb2, tag, tidx, pos, d, return_parts=True)
+    text = tag == synth.TAG_TEXT
+    np.testing.assert_array_equal(parts["xn"][text], parts2["xn"][text])
+    assert np.abs(parts["xn"][~text] - parts2["xn"][~text]).min() > 1.0
+
+
+def test_block_rows_subset_matches_full():
+    cfg, d, x, w, tb, tag, tidx, pos = _tiny_inputs()
+    full = O.block_forward(x, w, tb, tag, tidx, pos, d)
+    rows = np.array([0, 17, 40, 71])
+    sub = O.block_forward(x, w, tb, tag, tidx, pos, d, rows=rows)
+    np.testing.assert_allclose(sub, full[rows], rtol=0, atol=1e-12)
+
+
+def test_block_bf16_emulation_close_to_exact():
+    cfg, d, x, w, tb, tag, tidx, pos = _tiny_inputs()
+    a = O.block_forward(x, w, tb, tag, tidx, pos, d)
+    b = O.block_forward(x, w, tb, tag, tidx, pos, d, emulate_bf16=True)
+    rel = np.linalg.norm(a - b) / np.linalg.norm(a)
+    assert 0 < rel < 1e-2
+
+
+# ------------------------------------------------------------------------ work model
+
+
+def test_flop_model_matches_linear_share_on_the_pages():
+    g = _page("linear_share")
+    geo = _page("block_geometry")["value"]
+    assert (synth.H3.hidden, synth.H3.heads, synth.H3.head_dim, synth.H3.inner, synth.H3.ffn) == (
+        geo["hidden"], geo["heads"], geo["head_dim"], geo["inner"], geo["ffn"])
+    assert O.block_linear_params(synth.H3) == 385_351_680
+    for n, share in zip(g["rows"], g["value"]):
+        lin, att = O.block_flops(synth.H3, n)
+        assert abs(lin / (lin + att) - share) <= g["tolerance"], (n, lin / (lin + att))
