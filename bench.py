@@ -1,0 +1,363 @@
+#!/usr/bin/env python
+"""Benchmark: DiT trunk tokens/s per denoiser step on one B300 (plus attn+GEMM % of bf16 peak).
+
+A step is one denoiser evaluation of the 50-block H3 trunk (h3_trunk_forward) over the packed
+33,720-row sequence of a 768p 5 s Ref2VA request (text 256, one image condition 1,008, audio
+200, video 32x24x42), bf16 weights and activations, all inputs resident in HBM.  The
+modulation table (77 timesteps) is built once by h3_modcache_build before timing, as a run
+does.  Weights are random (seeded), so `data` is synthetic.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same workload (the path
+has no data-parallel split inside one forward); value is the whole-job tokens/s.
+`--impl reference` times the CPU oracle (the only reference implementation of this path) on a
+bounded sample of the same workload, on rank 0.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "DiT trunk tokens/s per denoiser step"
+UNIT = "tokens/s"
+CPU_SAMPLE_ROWS = 384
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def _flops(cfg, n_rows):
+    """(linear, attention) MMA FLOP of one block."""
+    d = cfg.dims
+    lin = 2 * n_rows * (3 * d.inner * d.hidden + d.hidden * d.inner + 2 * d.ffn * d.hidden + d.hidden * d.ffn)
+    return lin, 4 * n_rows * n_rows * d.inner
+
+
+# ------------------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id, rank):
+        self.bus = bus_id
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            sel = ["-i", self.bus] if self.bus else []
+            self.proc = subprocess.Popen(["nvidia-smi"] + sel + [f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle leg
+
+
+def cpu_oracle_sample(cfg, rows=CPU_SAMPLE_ROWS, step=10):
+    """Time the CPU oracle on one full-width block over `rows` rows sampled from the packed
+    sequence (same tags, positions and timestep mix), then scale by the FLOP model to the
+    whole trunk.  Returns (tokens/s, seconds, threads, description)."""
+    import oracle.h3_oracle as O
+
+    try:
+        from threadpoolctl import threadpool_info
+
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        threads = os.cpu_count() or 1
+    tag, tidx, pos = synth.packed_rows(cfg, step=step)
+    sel = np.sort(np.random.default_rng(0).choice(cfg.layout.n_rows, rows, replace=False))
+    sub = synth.Config(cfg.name + "_sample", cfg.dims, cfg.layout, cfg.seed, timesteps=cfg.timesteps,
+                       n_timesteps=cfg.n_timesteps)
+    x = synth.normal_bf16(cfg.seed, 0xABCD, (rows, cfg.dims.hidden))
+    w = synth.block_weights(sub, 0)
+    aw, ab = synth.adaln_weights(sub, 0)
+    used = np.unique(tidx[sel])
+    temb = synth.sinusoidal_temb(np.asarray(cfg.timesteps)[used], cfg.dims.temb_dim)
+    _, tbf = O.modcache(temb, [aw], [ab])
+    remap = {int(t): i for i, t in enumerate(used)}
+    tl = np.array([remap[int(t)] for t in tidx[sel]], np.int32)
+    t0 = time.perf_counter()
+    O.block_forward(x, w, tbf[:, 0, :], tag[sel], tl, pos[sel], cfg.dims)
+    dt = time.perf_counter() - t0
+    lin_s, att_s = _flops(cfg, rows)
+    rate = (lin_s + att_s) / dt
+    lin, att = _flops(cfg, cfg.layout.n_rows)
+    trunk_s = cfg.n_blocks * (lin + att) / rate
+    desc = (f"one full-width block over {rows} rows sampled from the {cfg.layout.n_rows}-row sequence, "
+            f"{dt:.2f} s ({rate / 1e9:.1f} GFLOP/s fp64); scaled by the FLOP model to {cfg.n_blocks} blocks "
+            f"at {cfg.layout.n_rows} rows")
+    return cfg.layout.n_rows / trunk_s, dt, threads, desc
+
+
+def run_reference(args, cfg, rank):
+    if rank != 0:
+        return
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, dt, threads, desc = cpu_oracle_sample(cfg)
+        if i >= args.warmup:
+            vals.append((v, dt))
+    value = statistics.median(v for v, _ in vals)
+    ms = statistics.median(cfg.layout.n_rows / v * 1e3 for v, _ in vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "rows": cfg.layout.n_rows, "blocks": cfg.n_blocks},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+
+    from joint_video_audio_block_b300 import h3
+    from joint_video_audio_block_b300 import runtime as R
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    d = cfg.dims
+    dims = R.dims_of(d)
+    N, B, T = cfg.layout.n_rows, args.blocks or cfg.n_blocks, cfg.n_timesteps
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    # weights (device-side seeded draws), modulation table built once, adaln weights dropped
+    blocks = [synth.device_block_weights(cfg, b) for b in range(B)]
+    temb = torch.from_numpy(synth.temb(cfg)).cuda()
+    table = torch.empty(T, B, 18 * d.hidden, dtype=torch.bfloat16, device=dev)
+    adaln = [synth.device_adaln_weights(cfg, b) for b in range(B)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    h3.h3_modcache_build(dims, temb.data_ptr(), T, d.temb_dim, [w.data_ptr() for w, _ in adaln],
+                         [b.data_ptr() for _, b in adaln], B, table.data_ptr(), sp)
+    e1.record()
+    torch.cuda.synchronize()
+    modcache_ms = e0.elapsed_time(e1)
+    modcache_bytes = B * 18 * d.hidden * (d.temb_dim + 1) * 2 + table.numel() * 2
+    del adaln
+    torch.cuda.empty_cache()
+
+    tag, tidx, pos = synth.packed_rows(cfg, step=10)
+    tag_d, tidx_d, pos_d = (torch.from_numpy(a).to(dev) for a in (tag, tidx, pos))
+    x0 = synth.device_normal_bf16(cfg.seed, 0xFFFF01, (N, d.hidden))
+    x = torch.empty_like(x0)
+    ws = R.workspace(dims, N)
+    bws = [h3.make_block_w(w) for w in blocks]
+
+    def step():
+        x.copy_(x0)
+        h3.h3_trunk_forward(dims, bws, B, table.data_ptr(), T, x.data_ptr(), N, tag_d.data_ptr(), tidx_d.data_ptr(),
+                            pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, site = h3.h3_last_device_error(sp)
+    if st != h3.H3_OK:
+        raise RuntimeError(f"device error after warm-up: {h3.h3_status_str(st)} site {site:#x}")
+
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+    except Exception:
+        bus = None
+    clocks = ClockSampler(bus, rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ta.record()
+    for _ in range(args.steps):
+        step()
+    tb.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    elapsed = ta.elapsed_time(tb) / 1e3
+    if dist:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    st, site = h3.h3_last_device_error(sp)
+    if st != h3.H3_OK:
+        raise RuntimeError(f"device error in timed region: site {site:#x}")
+    ms_per_step = elapsed / args.steps * 1e3
+    value = world * N * args.steps / elapsed
+
+    # end to end: host (pinned) inputs in, result out, every step
+    xh = x0.cpu().pin_memory()
+    out_h = torch.empty_like(xh).pin_memory()
+    tag_h, tidx_h, pos_h = (torch.from_numpy(a).pin_memory() for a in (tag, tidx, pos))
+    h2d = xh.numel() * 2 + tag_h.numel() + tidx_h.numel() * 4 + pos_h.numel() * 4
+    d2h = out_h.numel() * 2
+
+    def e2e_step():
+        x.copy_(xh, non_blocking=True)
+        tag_d.copy_(tag_h, non_blocking=True)
+        tidx_d.copy_(tidx_h, non_blocking=True)
+        pos_d.copy_(pos_h, non_blocking=True)
+        h3.h3_trunk_forward(dims, bws, B, table.data_ptr(), T, x.data_ptr(), N, tag_d.data_ptr(), tidx_d.data_ptr(),
+                            pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp)
+        out_h.copy_(x, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * N * args.steps / e2e_s
+
+    # dominant kernel: attention at the workload's shape, timed alone on the same stream
+    ld_vt = (N + 63) // 64 * 64
+    qa = synth.device_normal_bf16(cfg.seed, 0xA1, (d.heads, N, d.head_dim))
+    ka = synth.device_normal_bf16(cfg.seed, 0xA2, (d.heads, N, d.head_dim))
+    va = synth.device_normal_bf16(cfg.seed, 0xA3, (d.heads, d.head_dim, ld_vt))
+    oa = torch.empty(N, d.inner, dtype=torch.bfloat16, device=dev)
+    reps = 5
+    h3.h3_attention(dims, qa.data_ptr(), ka.data_ptr(), va.data_ptr(), ld_vt, oa.data_ptr(), N, 0, sp)
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record()
+    for _ in range(reps):
+        h3.h3_attention(dims, qa.data_ptr(), ka.data_ptr(), va.data_ptr(), ld_vt, oa.data_ptr(), N, 0, sp)
+    eb.record()
+    torch.cuda.synchronize()
+    att_s = ea.elapsed_time(eb) / 1e3 / reps
+    hbm_peak, bf16_peak, bf16_sus, peak_kind = _peaks()
+    lin_f, att_f = _flops(cfg, N)
+    att_tflops = att_f / att_s / 1e12
+    mma_tflops = B * (lin_f + att_f) / (ms_per_step / 1e3) / 1e12  # per GPU (each replica)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, threads, desc = cpu_oracle_sample(cfg)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "rows": N, "blocks": B, "hidden": d.hidden, "heads": d.heads,
+                       "head_dim": d.head_dim, "ffn": d.ffn, "timesteps_in_table": T,
+                       "l2": "inputs larger than L2 (38.5 GB of weights streamed per step)",
+                       "parallelism": f"replicas{world}"},
+            "mma_frac_of_bf16_peak": {"tflops": mma_tflops, "burst": mma_tflops / bf16_peak,
+                                      "sustained": mma_tflops / bf16_sus, "peak_kind": peak_kind},
+            "roofline": {"kernel": "attention_tc_kernel<128>", "bound": "tensor", "achieved": att_tflops,
+                         "peak": bf16_peak, "unit": "TFLOP/s", "frac": att_tflops / bf16_peak,
+                         "peak_kind": f"{peak_kind} bf16 burst", "traffic": None,
+                         "flop_per_launch": att_f, "ms_per_launch": att_s * 1e3},
+            "modcache": {"ms": modcache_ms, "timesteps": T, "blocks": B,
+                         "GB_per_s": modcache_bytes / (modcache_ms / 1e3) / 1e9},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * (1 + 8 * B),
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="trunk33720")
+    ap.add_argument("--blocks", type=int, default=0, help="override the block count (diagnostics only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = synth.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+    run_ours(args, cfg, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * libh3 -- the denoiser forward of the H3 joint audio+video DiT trunk on one B300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument named "device" is a CUDA device pointer owned by the caller;
+ * pointers named "host" are host memory.  The library allocates no device memory: scratch
+ * space comes from the caller's workspace.  All compute calls are asynchronous on `stream`
+ * (a cudaStream_t passed as void*; NULL = the legacy default stream) and return before the
+ * GPU work finishes.  Tensors are dense and row-major unless a stride is given; "bf16" means
+ * IEEE bfloat16 bit patterns (2 bytes), "f32" float32.
+ *
+ * Errors: every call returns an h3_status.  Shape, alignment and null-pointer violations are
+ * detected on the host and return H3_EINVAL before anything is launched; a CUDA launch error
+ * returns H3_ECUDA.  Kernels never trap: a pipeline wait that exceeds its time limit records a
+ * site code in the library's device error word and ends the launch; h3_last_device_error()
+ * reports it.  Nothing aborts the process.
+ *
+ * Sources (page and section): "minimax-h3-mlx" README -- "Architecture" (packed sequence
+ * [text | conditions | audio | video], per-row AdaLN modality tag, 50 blocks, hidden 5376,
+ * 56 x 128 heads, SwiGLU 14336, 3D MM-RoPE), "AdaLN precompute" (ModulationCache,
+ * adaln_proj 50 x [96768, 2688]), "AdaLN: measure, do not reason" (six modulation tensors,
+ * x*(1+scale)+shift, x + gate*f(x)), "Validation" (per-head interleaved qkv rows, fused
+ * [gate; value] fc1); "H3-metal" README -- "Exact DiT fusions", "Checkpoint layout and media
+ * pipeline" (fused QK-norm + RoPE on interleaved qkv); "mlx-h3" README -- "Local model
+ * layout" (weight-only INT8 group 32).
+ */
+#ifndef H3_H
+#define H3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  H3_OK = 0,
+  H3_EINVAL = 1,        /* bad shape, alignment, pointer or argument */
+  H3_EUNSUPPORTED = 2,  /* valid request this build does not implement */
+  H3_ECUDA = 3,         /* CUDA runtime / driver call failed */
+  H3_ETIMEOUT = 4       /* a device pipeline wait ran out (see h3_last_device_error) */
+} h3_status;
+
+typedef enum { H3_W_BF16 = 0, H3_W_INT8_G32 = 1 } h3_wfmt;
+
+/* flags for the block / trunk calls */
+#define H3_F_UNFUSED 0x1u      /* run the plain CUDA-core reference kernels instead of tcgen05 */
+#define H3_F_NO_QKNORM 0x2u    /* skip QK RMSNorm even if weights are given */
+#define H3_F_CHECK_INDEX 0x4u  /* copy tag/tidx to the host and range-check them first (synchronises) */
+
+/* Block geometry.  hidden H, heads nh, head_dim hd (64 or 128), ffn F, n_tags modality tags.
+ * rope_sections: frequency pairs given to the (t, h, w) position axes, summing to hd/2.
+ * Requirements: H % 64 == 0, (nh*hd) % 64 == 0, F % 128 == 0. */
+typedef struct {
+  int hidden, heads, head_dim, ffn, n_tags;
+  int rope_sections[3];
+  float rope_theta; /* 1e4 */
+  float ln_eps;     /* LayerNorm eps, 1e-6 */
+  float qk_eps;     /* QK RMSNorm eps, 1e-6 */
+} h3_dims;
+
+/* One linear layer y = x W^T + b with W [n_out, k] (checkpoint orientation).
+ * H3_W_BF16:     w = device bf16 [n_out, k].
+ * H3_W_INT8_G32: w = device u8 codes [n_out, k]; scale, qbias = device bf16 [n_out, k/32];
+ *                W[o][c] = bf16(fma_f32(scale[o][c/32], w[o][c], qbias[o][c/32])); k % 32 == 0.
+ * bias: device bf16 [n_out] or NULL.  Row strides must be multiples of 16 bytes. */
+typedef struct {
+  int fmt;
+  const void* w;
+  const void* scale;
+  const void* qbias;
+  const void* bias;
+  int n_out, k;
+} h3_linear;
+
+/* One block's weights.  qkv: [3*nh*hd, H], rows interleaved per head ([h: q, k, v]);
+ * o: [H, nh*hd]; fc1: [2F, H], first F rows = gate; fc2: [H, F].
+ * q_norm, k_norm: device bf16 [hd] RMSNorm weights or NULL (no QK-norm). */
+typedef struct {
+  h3_linear qkv, o, fc1, fc2;
+  const void* q_norm;
+  const void* k_norm;
+} h3_block_w;
+
+/* Modulation table addressing.  The table holds, per timestep t and block b, 18*H bf16 values
+ * read as 3 modality tags x 6 tensors x H, tensor order (shift_msa, scale_msa, gate_msa,
+ * shift_mlp, scale_mlp, gate_mlp): entry (t, b, tag, m, c) is at
+ *   table[t*t_stride + b*18*H + (6*tag + m)*H + c].
+ * h3_modcache_build writes the packed layout [T][B][18][H] (t_stride = B*18*H). */
+
+/* Bytes of workspace h3_block_forward / h3_trunk_forward need for n_rows rows. */
+size_t h3_workspace_size(const h3_dims* dims, int n_rows);
+
+/* a0 -- ModulationCache build ("minimax-h3-mlx" README, "AdaLN precompute").
+ *   table[t][b][j] = bf16( sum_k adaln_w[b][j][k] * temb[t][k] + adaln_b[b][j] ),
+ * fp32 accumulation, j < 18*H.
+ * temb: device f32 [T, Dt]; adaln_w: HOST array of n_blocks device pointers to bf16 [18H, Dt];
+ * adaln_b: HOST array of n_blocks device pointers to bf16 [18H] (array or entries may be NULL);
+ * table: device bf16 [T][n_blocks][18H], written.  Dt % 8 == 0. */
+h3_status h3_modcache_build(const h3_dims* dims, const float* temb, int T, int Dt, const void* const* adaln_w,
+                            const void* const* adaln_b, int n_blocks, void* table, void* stream);
+
+/* a1..a8 -- one DiT block over the packed sequence.
+ * table_b: device pointer to this block's slice at t = 0 (table + b*18*H), t_stride as above,
+ * T timesteps.  x_in, x_out: device bf16 [n_rows, H] (x_out may equal x_in; otherwise they must
+ * not overlap).  tag: device u8 [n_rows] (< n_tags); tidx: device i32 [n_rows] (< T);
+ * pos: device f32 [n_rows, 3] = (t, h, w) rotary position (1-D rows pass (p, p, p)).
+ * workspace: device, >= h3_workspace_size bytes, 256-byte aligned. */
+h3_status h3_block_forward(const h3_dims* dims, const h3_block_w* w, const void* table_b, long long t_stride, int T,
+                           const void* x_in, void* x_out, int n_rows, const uint8_t* tag, const int32_t* tidx,
+                           const float* pos, void* workspace, size_t ws_bytes, unsigned flags, void* stream);
+
+/* a10 -- the trunk: for b < n_blocks, x = block_b(x; table[:, b]).  blocks: HOST array of
+ * n_blocks weight sets; table: device bf16 [T][n_blocks][18H] as written by h3_modcache_build;
+ * x: device bf16 [n_rows, H], updated in place.  Other arguments as h3_block_forward.  The
+ * rotary cos/sin table is computed once per call and shared by all blocks. */
+h3_status h3_trunk_forward(const h3_dims* dims, const h3_block_w* blocks, int n_blocks, const void* table, int T,
+                           void* x, int n_rows, const uint8_t* tag, const int32_t* tidx, const float* pos,
+                           void* workspace, size_t ws_bytes, unsigned flags, void* stream);
+
+/* ---- step entry points (each row of the block on its own; used for per-step parity) ---- */
+
+/* a1 / a6 -- gather + LayerNorm + modulate ("minimax-h3-mlx" README, "AdaLN: measure, do not
+ * reason"): xn[r] = LN(x[r]) * (1 + table_b[tidx[r]*t_stride + (6 tag[r] + m_scale) H])
+ *                            + table_b[tidx[r]*t_stride + (6 tag[r] + m_shift) H].
+ * LayerNorm without affine, biased variance, eps = dims->ln_eps; statistics in fp32.
+ * x, xn: device bf16 [n_rows, H] (distinct). */
+h3_status h3_adaln_modulate(const h3_dims* dims, const void* x, void* xn, int n_rows, const void* table_b,
+                            long long t_stride, int m_shift, int m_scale, const uint8_t* tag, const int32_t* tidx,
+                            void* stream);
+
+/* epilogues of h3_linear_forward */
+#define H3_EPI_BIAS 0      /* y = x W^T + b                                                   */
+#define H3_EPI_SWIGLU 1    /* y = silu(g) * v, [g | v] = x W^T + b, W has 2*n_out rows (gate first) */
+#define H3_EPI_GATE_RES 2  /* y = res + gate(r) * (x W^T + b), gate from the modulation table */
+
+/* a2 / a5 / a7 / a8 / a9 -- one linear with a fused epilogue on the tcgen05 tensor cores.
+ * x: device bf16 [n_rows, lin->k] (row stride lda elements); y: device bf16 [n_rows, n_y]
+ * (row stride ldy), n_y = lin->n_out except SWIGLU where n_y = lin->n_out / 2.
+ * GATE_RES: res device bf16 [n_rows, n_y] (stride ldy; may equal y), the gate of row r and
+ * column c is table_b[tidx[r]*t_stride + (6 tag[r] + m_gate) n_y + c].  Unused arguments may
+ * be NULL / 0.  flags: H3_F_UNFUSED selects the CUDA-core reference GEMM. */
+h3_status h3_linear_forward(const h3_linear* lin, int epilogue, const void* x, int lda, void* y, int ldy,
+                            int n_rows, const void* res, const void* table_b, long long t_stride, int m_gate,
+                            const uint8_t* tag, const int32_t* tidx, unsigned flags, void* stream);
+
+/* a3 -- QK RMSNorm + 3D MM-RoPE on the interleaved projection ("H3-metal" README,
+ * "Checkpoint layout and media pipeline"): for row r, head h, q = qkv[r, h*3hd + 0..hd),
+ * k = qkv[r, h*3hd + hd..2hd), v = qkv[r, h*3hd + 2hd..3hd); q, k <- RMSNorm(.) * w (if weights
+ * given), then rotate-half RoPE with angle pos[r][axis(i)] * theta^(-2i/hd) for pair (i, i+hd/2),
+ * axis(i) by rope_sections.  Outputs head-major q_out, k_out: device bf16 [nh][n_rows][hd];
+ * vt_out: device bf16 [nh][hd][ld_vt] (v transposed, ld_vt >= n_rows, ld_vt % 8 == 0).
+ * workspace: device scratch of >= n_rows * hd/2 * 8 bytes (the per-row cos/sin table). */
+h3_status h3_qknorm_rope(const h3_dims* dims, const void* qkv, const float* pos, const void* q_norm,
+                         const void* k_norm, void* q_out, void* k_out, void* vt_out, int ld_vt, int n_rows,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* a4 -- full unmasked self-attention ("minimax-h3-mlx" README, "Architecture"): per head,
+ * o[r, h*hd + d] = sum_j softmax_j(q[h][r] . k[h][j] / sqrt(hd)) vt[h][d][j] over all j < n_rows.
+ * q, k: device bf16 [nh][n_rows][hd]; vt: device bf16 [nh][hd][ld_vt]; o: device bf16
+ * [n_rows, nh*hd].  hd must be 128 on the tcgen05 path.  flags: H3_F_UNFUSED = reference kernel. */
+h3_status h3_attention(const h3_dims* dims, const void* q, const void* k, const void* vt, int ld_vt, void* o,
+                       int n_rows, unsigned flags, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device error word.  Returns H3_OK, or
+ * H3_ETIMEOUT when a bounded device wait ran out since the last call (*site, if not NULL,
+ * receives the site code), or H3_ECUDA if the stream reports a CUDA error. */
+h3_status h3_last_device_error(void* stream, unsigned* site);
+
+const char* h3_status_str(h3_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3_H */

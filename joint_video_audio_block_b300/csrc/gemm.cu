@@ -1,0 +1,483 @@
+// a2 / a5 / a7 / a8 / a9: the trunk linears on the 5th-generation tensor cores.
+//
+// y[M, n] = epilogue(x[M, K] . W[n, K]^T + b), x and W both K-major bf16 (or W as weight-only
+// INT8 group-32 codes, "mlx-h3" README, "Local model layout"), fp32 accumulation in TMEM.
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: A tile 128x64 and B tile 256x64 per stage (128-byte swizzle)
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128, N=256, K=16 steps)
+//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bias / SwiGLU / gate+residual, store
+//   warps 6..9  (INT8 only) dequantise the u8 codes of each stage into the swizzled bf16 B tile
+// Two 256-column accumulators in TMEM let the epilogue of tile i overlap the mainloop of i+1.
+//
+// Epilogues ("minimax-h3-mlx" README, "Validation" and "AdaLN: measure, do not reason";
+// "H3-metal" README, "Metal 4 and TensorOps paths" for the paired gate/up tiles):
+//   BIAS     y = acc + b
+//   SWIGLU   the B tile is the gate rows j..j+127 and the value rows F+j..F+j+127, so one
+//            256-wide accumulator holds both halves and y = silu(g + b_g) * (v + b_v) is
+//            formed on-chip; only the F-wide activation is written
+//   GATE_RES y = res + gate[tag, t] * (acc + b), the AdaLN gate gathered per row
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+
+namespace h3 {
+
+constexpr int G_BM = 128, G_BN = 256, G_BK = 64;
+constexpr int G_A_BYTES = G_BM * G_BK * 2;   // 16 KB
+constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
+constexpr int G_Q_BYTES = G_BN * G_BK;       // 16 KB of u8 codes (INT8 path)
+constexpr int GROUP_M = 16;                  // tile raster: 16 row-blocks per column sweep
+
+template <bool INT8>
+struct GemmCfg {
+  static constexpr int STAGES = 4 - (INT8 ? 1 : 0);
+  static constexpr int STAGE_BYTES = G_A_BYTES + G_B_BYTES + (INT8 ? G_Q_BYTES : 0);
+  static constexpr int THREADS = INT8 ? 320 : 192;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+struct GemmParams {
+  int M, K, n_y;
+  int m_tiles, n_tiles, num_tiles, kb_count;
+  int b_row_step;   // B rows per column tile: 256 (plain) or 128 (SwiGLU)
+  int b_row1_off;   // row offset of the second 128-row half of a B tile: 128, or n_y for SwiGLU
+  const bf16* bias;
+  bf16* y;
+  int ldy;
+  const bf16* res;
+  TableRef gate;
+  int m_gate;
+  const bf16* wscale;  // INT8: [rows, K/32]
+  const bf16* wqbias;
+  int groups;          // K / 32
+  unsigned* err;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int& mb, int& nb) {
+  const int per_group = GROUP_M * n_tiles;
+  const int g = tile / per_group;
+  const int first_m = g * GROUP_M;
+  const int gm = min(m_tiles - first_m, GROUP_M);
+  const int local = tile % per_group;
+  mb = first_m + local % gm;
+  nb = local / gm;
+}
+
+__device__ __forceinline__ void load8(const bf16* p, float* f) {
+  const int4 u = ld_nc_v4(p);
+  const uint32_t w[4] = {(uint32_t)u.x, (uint32_t)u.y, (uint32_t)u.z, (uint32_t)u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16lo(w[i]);
+    f[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ void store_row32(bf16* dst, const float* v, int valid) {
+  if (valid >= 32) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int4 o = make_int4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                               pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+      reinterpret_cast<int4*>(dst)[c] = o;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) dst[i] = f2bf(v[i]);
+  }
+}
+
+// Epilogue of one tile for the calling thread's row (TMEM lane = row within the tile).
+template <int EPI>
+__device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc, int row, int nb) {
+  const bool row_ok = row < p.M;
+  if (EPI == kEpiSwiglu) {
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t rg[32], rv[32];
+      tmem_ld32(tacc + c * 32, rg);
+      tmem_ld32(tacc + 128 + c * 32, rv);
+      tmem_wait_ld();
+      const int col0 = nb * 128 + c * 32;
+      if (row_ok && col0 < p.n_y) {
+        float v[32];
+        const int valid = min(32, p.n_y - col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float bg[8], bv[8];
+          if (p.bias && valid >= 32) {
+            load8(p.bias + col0 + 8 * q, bg);
+            load8(p.bias + p.n_y + col0 + 8 * q, bv);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int cc = col0 + 8 * q + e;
+              bg[e] = (p.bias && cc < p.n_y) ? bf2f(p.bias[cc]) : 0.f;
+              bv[e] = (p.bias && cc < p.n_y) ? bf2f(p.bias[p.n_y + cc]) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float g = __uint_as_float(rg[8 * q + e]) + bg[e];
+            const float u = __uint_as_float(rv[8 * q + e]) + bv[e];
+            v[8 * q + e] = g / (1.f + expf(-g)) * u;
+          }
+        }
+        store_row32(p.y + static_cast<size_t>(row) * p.ldy + col0, v, valid);
+      }
+    }
+  } else {
+    const bf16* gate_row = nullptr;
+    if (EPI == kEpiGateRes && row_ok) {
+      const TableRef& t = p.gate;
+      gate_row = t.table_b + static_cast<long long>(t.tidx[row]) * t.t_stride +
+                 static_cast<long long>(6 * t.tag[row] + p.m_gate) * p.n_y;
+    }
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c * 32, r);
+      tmem_wait_ld();
+      const int col0 = nb * 256 + c * 32;
+      if (row_ok && col0 < p.n_y) {
+        const int valid = min(32, p.n_y - col0);
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float b[8], rs[8], g[8];
+          if (valid >= 32) {
+            if (p.bias) load8(p.bias + col0 + 8 * q, b);
+            else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) b[e] = 0.f;
+            }
+            if (EPI == kEpiGateRes) {
+              load8(p.res + static_cast<size_t>(row) * p.ldy + col0 + 8 * q, rs);
+              load8(gate_row + col0 + 8 * q, g);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int cc = col0 + 8 * q + e;
+              const bool ok = cc < p.n_y;
+              b[e] = (p.bias && ok) ? bf2f(p.bias[cc]) : 0.f;
+              if (EPI == kEpiGateRes) {
+                rs[e] = ok ? bf2f(p.res[static_cast<size_t>(row) * p.ldy + cc]) : 0.f;
+                g[e] = ok ? bf2f(gate_row[cc]) : 0.f;
+              }
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float a = __uint_as_float(r[8 * q + e]) + b[e];
+            v[8 * q + e] = (EPI == kEpiGateRes) ? rs[e] + g[e] * a : a;
+          }
+        }
+        store_row32(p.y + static_cast<size_t>(row) * p.ldy + col0, v, valid);
+      }
+    }
+  }
+}
+
+// Dequantise one stage: u8 codes [256][64] (row-major, no swizzle) -> bf16 [256][64] in the
+// 128-byte swizzled K-major layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).
+// Thread t of the 128 dequant threads handles k-chunk (t & 3) (16 codes, one group) of rows
+// t/4 + 32 i; a warp therefore reads 512 contiguous code bytes per step.
+__device__ __forceinline__ void dequant_stage(const uint8_t* sq, uint8_t* sb, const GemmParams& p, int brow0, int brow1,
+                                              int kb, int t) {
+  const int kc = t & 3;
+  const int g = kb * 2 + (kc >> 1);
+#pragma unroll 2
+  for (int i = 0; i < 8; ++i) {
+    const int n = (t >> 2) + 32 * i;                  // row within the 256-row tile
+    const int grow = (n < 128) ? brow0 + n : brow1 + (n - 128);
+    float sc = 0.f, qb = 0.f;
+    if (g < p.groups) {
+      const size_t gi = static_cast<size_t>(grow) * p.groups + g;
+      sc = bf2f(p.wscale[gi]);
+      qb = bf2f(p.wqbias[gi]);
+    }
+    const int4 codes = *reinterpret_cast<const int4*>(sq + n * 64 + kc * 16);
+    const uint32_t cw[4] = {(uint32_t)codes.x, (uint32_t)codes.y, (uint32_t)codes.z, (uint32_t)codes.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t b0 = (cw[w] >> (16 * h)) & 0xFFu, b1 = (cw[w] >> (16 * h + 8)) & 0xFFu;
+        // exact u8 -> f32 through the 2^23 magic constant
+        const float f0 = __uint_as_float(0x4B000000u | b0) - 8388608.f;
+        const float f1 = __uint_as_float(0x4B000000u | b1) - 8388608.f;
+        o[2 * w + h] = pack_bf16x2(__fmaf_rn(sc, f0, qb), __fmaf_rn(sc, f1, qb));
+      }
+    }
+    uint8_t* rowp = sb + n * 128;
+    const int c0 = 2 * kc, c1 = 2 * kc + 1;
+    *reinterpret_cast<int4*>(rowp + ((c0 ^ (n & 7)) << 4)) = make_int4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<int4*>(rowp + ((c1 ^ (n & 7)) << 4)) = make_int4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+template <int EPI, bool INT8>
+__global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  using C = GemmCfg<INT8>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  const uint32_t bar_full = smem_u32(bars);          // S barriers: TMA landed
+  const uint32_t bar_empty = bar_full + 8 * S;       // S barriers: MMA done with the stage
+  const uint32_t bar_ready = bar_empty + 8 * S;      // S barriers: INT8 dequant done
+  const uint32_t bar_tfull = bar_ready + 8 * S;      // 2 barriers: accumulator complete
+  const uint32_t bar_tempty = bar_tfull + 16;        // 2 barriers: accumulator drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_ready + 8 * s, 4);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, 4);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto sA = [&](int s) { return smem + s * C::STAGE_BYTES; };
+  auto sB = [&](int s) { return smem + s * C::STAGE_BYTES + G_A_BYTES; };
+  auto sQ = [&](int s) { return smem + s * C::STAGE_BYTES + G_A_BYTES + G_B_BYTES; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
+        const int brow0 = nb * p.b_row_step, brow1 = brow0 + p.b_row1_off;
+        for (int kb = 0; kb < p.kb_count; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, p.err, kErrGemmProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * s;
+          mbar_arrive_expect_tx(fb, G_A_BYTES + (INT8 ? G_Q_BYTES : G_B_BYTES));
+          tma_load_2d(smem_u32(sA(s)), &tmA, fb, kb * G_BK, mb * G_BM);
+          if (INT8) {
+            tma_load_2d(smem_u32(sQ(s)), &tmB, fb, kb * G_BK, brow0);
+            tma_load_2d(smem_u32(sQ(s)) + 128 * 64, &tmB, fb, kb * G_BK, brow1);
+          } else {
+            tma_load_2d(smem_u32(sB(s)), &tmB, fb, kb * G_BK, brow0);
+            tma_load_2d(smem_u32(sB(s)) + 128 * 128, &tmB, fb, kb * G_BK, brow1);
+          }
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(G_BM, G_BN);
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1, p.err, kErrGemmMma)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * G_BN;
+        for (int kb = 0; kb < p.kb_count; ++kb) {
+          if (!mbar_wait((INT8 ? bar_ready : bar_full) + 8 * s, ph, p.err, kErrGemmMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA(s)), b0 = smem_u32(sB(s));
+#pragma unroll
+          for (int k = 0; k < G_BK / 16; ++k)
+            umma_bf16_ss(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
+          umma_commit(bar_empty + 8 * s);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(bar_tfull + 8 * acc);
+        acc ^= 1;
+        if (acc == 0) aph ^= 1;
+      }
+    }
+  } else if (warp < 6) {
+    const int quad = warp & 3;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
+      if (!mbar_wait(bar_tfull + 8 * acc, aph, p.err, kErrGemmEpilogue)) break;
+      tc_fence_after();
+      const int row = mb * G_BM + quad * 32 + lane;
+      gemm_epilogue<EPI>(p, tmem_base + acc * G_BN + ((quad * 32) << 16), row, nb);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1;
+    }
+  } else if (INT8) {
+    const int t = threadIdx.x - 192;  // 0..127
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
+      const int brow0 = nb * p.b_row_step, brow1 = brow0 + p.b_row1_off;
+      for (int kb = 0; kb < p.kb_count; ++kb) {
+        if (!mbar_wait(bar_full + 8 * s, ph, p.err, kErrGemmDequant)) {
+          ok = false;
+          break;
+        }
+        dequant_stage(sQ(s), sB(s), p, brow0, brow1, kb, t);
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ready + 8 * s);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+
+CUresult tensor_map_encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank, void* addr,
+                                 const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                                 const cuuint32_t* estr, CUtensorMapInterleave il, CUtensorMapSwizzle sw,
+                                 CUtensorMapL2promotion l2, CUtensorMapFloatOOBfill oob) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return CUDA_ERROR_NOT_FOUND;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn(m, dt, rank, addr, dims, strides, box, estr, il, sw, l2, oob);
+}
+
+static bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = tensor_map_encode_tiled(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                                      CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+template <int EPI, bool INT8>
+static cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st) {
+  using C = GemmCfg<INT8>;
+  static bool configured = false;  // per instantiation; the attribute is per function, not per device
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, INT8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = min(p.num_tiles, num_sms());
+  gemm_tc_kernel<EPI, INT8><<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
+  if (a.M <= 0) return cudaSuccess;
+  GemmParams p{};
+  p.M = a.M;
+  p.K = a.K;
+  p.n_y = a.n_y;
+  p.m_tiles = cdiv(a.M, G_BM);
+  const bool sw = a.epi == kEpiSwiglu;
+  p.b_row_step = sw ? 128 : 256;
+  p.b_row1_off = sw ? a.n_y : 128;
+  p.n_tiles = cdiv(a.n_y, p.b_row_step);
+  p.num_tiles = p.m_tiles * p.n_tiles;
+  p.kb_count = cdiv(a.K, G_BK);
+  p.bias = a.bias;
+  p.y = a.y;
+  p.ldy = a.ldy;
+  p.res = a.res;
+  p.gate = a.gate;
+  p.m_gate = a.m_gate;
+  p.wscale = a.wscale;
+  p.wqbias = a.wqbias;
+  p.groups = a.K / 32;
+  p.err = a.err;
+  const int w_rows = sw ? 2 * a.n_y : a.n_y;
+
+  CUtensorMap ta, tb;
+  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, static_cast<uint64_t>(a.lda) * 2, G_BK, G_BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (a.int8) {
+    if (!encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w, a.K, w_rows, static_cast<uint64_t>(a.K), G_BK, 128,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w, a.K, w_rows, static_cast<uint64_t>(a.K) * 2, G_BK, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  switch (a.epi * 2 + (a.int8 ? 1 : 0)) {
+    case kEpiBias * 2: return launch_tc<kEpiBias, false>(ta, tb, p, st);
+    case kEpiBias * 2 + 1: return launch_tc<kEpiBias, true>(ta, tb, p, st);
+    case kEpiSwiglu * 2: return launch_tc<kEpiSwiglu, false>(ta, tb, p, st);
+    case kEpiSwiglu * 2 + 1: return launch_tc<kEpiSwiglu, true>(ta, tb, p, st);
+    case kEpiGateRes * 2: return launch_tc<kEpiGateRes, false>(ta, tb, p, st);
+    case kEpiGateRes * 2 + 1: return launch_tc<kEpiGateRes, true>(ta, tb, p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace h3

@@ -1,0 +1,68 @@
+// Internal launcher declarations shared by the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include "common.cuh"
+
+namespace h3 {
+
+// A row's modulation vector m lives at table_b[tidx[r]*t_stride + (6*tag[r] + m)*H + c].
+struct TableRef {
+  const bf16* table_b;
+  long long t_stride;
+  const uint8_t* tag;
+  const int32_t* tidx;
+};
+
+enum Epilogue : int { kEpiBias = 0, kEpiSwiglu = 1, kEpiGateRes = 2 };
+
+// y = epilogue(x W^T + b).  W is bf16 [n_w_rows, K] or INT8-g32 codes + per-group scale/qbias.
+struct LinearArgs {
+  const bf16* x;
+  int lda;
+  int M;        // rows of x
+  int K;        // reduction length
+  int n_y;      // output columns (n_out, or n_out/2 for SwiGLU)
+  bool int8;
+  const void* w;         // bf16 [n_w_rows, K] or u8 [n_w_rows, K]
+  const bf16* wscale;    // int8: [n_w_rows, K/32]
+  const bf16* wqbias;    // int8: [n_w_rows, K/32]
+  const bf16* bias;      // [n_w_rows] or null
+  bf16* y;
+  int ldy;
+  int epi;
+  const bf16* res;       // gate-residual input (stride ldy)
+  TableRef gate;         // gate-residual gate
+  int m_gate;
+  unsigned* err;
+};
+
+cudaError_t launch_adaln_modulate(const bf16* x, bf16* xn, int n_rows, int H, float eps, TableRef tr, int m_shift,
+                                  int m_scale, cudaStream_t st);
+
+cudaError_t launch_rope_table(const float* pos, float2* cs, int n_rows, int hd, const int sections[3], float theta,
+                              cudaStream_t st);
+
+cudaError_t launch_qknorm_rope(const bf16* qkv, const float2* cs, const bf16* qn, const bf16* kn, float eps, bf16* q,
+                               bf16* k, bf16* vt, int ld_vt, int n_rows, int nh, int hd, cudaStream_t st);
+
+cudaError_t launch_modcache(const float* temb, int T, int Dt, const bf16* W, const bf16* bias, int n_out,
+                            bf16* table_b, long long t_stride, cudaStream_t st);
+
+cudaError_t launch_linear_ref(const LinearArgs& a, cudaStream_t st);
+cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st);
+
+cudaError_t launch_attention_ref(const bf16* q, const bf16* k, const bf16* vt, int ld_vt, bf16* o, int n_rows, int nh,
+                                 int hd, cudaStream_t st);
+cudaError_t launch_attention_tc(const bf16* q, const bf16* k, const bf16* vt, int ld_vt, bf16* o, int n_rows, int nh,
+                                int hd, unsigned* err, cudaStream_t st);
+
+int num_sms();
+
+// cuTensorMapEncodeTiled fetched through the runtime's driver entry point (the library does not
+// link libcuda directly, so it loads on machines without a driver).
+CUresult tensor_map_encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, cuuint32_t rank, void* addr,
+                                 const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                                 const cuuint32_t* estr, CUtensorMapInterleave il, CUtensorMapSwizzle sw,
+                                 CUtensorMapL2promotion l2, CUtensorMapFloatOOBfill oob);
+
+}  // namespace h3

@@ -355,3 +355,44 @@ def quantize_int8_g32(w_bits: np.ndarray):
     t = np.where(scale[:, :, None] == 0, 0.0, t).astype(np.float32)
     q = np.clip(np.rint(t), 0, 255).astype(np.uint8)
     return q.reshape(n, k), scale_bits, qb_bits
+
+
+# --------------------------------------------------------------------------------------
+# bulk device-side draws (benchmark weights only)
+# --------------------------------------------------------------------------------------
+
+
+def device_normal_bf16(seed: int, stream: int, shape, mean: float = 0.0, std: float = 1.0, device="cuda"):
+    """N(mean, std^2) bf16 tensor drawn on the device by torch's seeded Philox generator.
+
+    Used only to fill the 50-block benchmark trunk quickly (tens of GB); these values are not
+    the ones the host generator above produces, and no parity test uses them.
+    """
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed((seed * 0x9E3779B1 + stream * 0x85EBCA77) & 0x7FFFFFFFFFFFFFFF)
+    t = torch.empty(shape, dtype=torch.float32, device=device)
+    t.normal_(mean, std, generator=g)
+    return t.to(torch.bfloat16)
+
+
+def device_block_weights(cfg: Config, block: int, device="cuda") -> dict:
+    """One block's weights (shapes and distributions of block_weights) drawn on the device."""
+    d = cfg.dims
+    H, I, F, hd = d.hidden, d.inner, d.ffn, d.head_dim
+    s = cfg.seed
+    spec = {
+        "wqkv": ((3 * I, H), 0.0, _T_WQKV), "bqkv": ((3 * I,), 0.0, _T_BQKV), "wo": ((H, I), 0.0, _T_WO),
+        "bo": ((H,), 0.0, _T_BO), "w1": ((2 * F, H), 0.0, _T_W1), "b1": ((2 * F,), 0.0, _T_B1),
+        "w2": ((H, F), 0.0, _T_W2), "b2": ((H,), 0.0, _T_B2), "qnorm": ((hd,), 1.0, _T_QN), "knorm": ((hd,), 1.0, _T_KN),
+    }
+    return {k: device_normal_bf16(s, _stream(block, tid), shp, mu, 0.02, device) for k, (shp, mu, tid) in spec.items()}
+
+
+def device_adaln_weights(cfg: Config, block: int, device="cuda"):
+    d = cfg.dims
+    s = cfg.seed
+    W = device_normal_bf16(s, _stream(block, _T_AW), (18 * d.hidden, d.temb_dim), 0.0, 0.02, device)
+    b = device_normal_bf16(s, _stream(block, _T_AB), (18 * d.hidden,), 0.0, 0.02, device)
+    return W, b

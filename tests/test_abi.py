@@ -1,0 +1,94 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point include/h3.h declares,
+and its host-side logic (workspace plan, argument checks, status strings) behaves."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "h3.h")
+
+
+@pytest.fixture(scope="module")
+def h3mod():
+    from joint_video_audio_block_b300 import build
+
+    build.build()
+    from joint_video_audio_block_b300 import h3
+
+    h3.lib()
+    return h3
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:h3_status|size_t|const char\s*\*)\s+(h3_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("h3_modcache_build", "h3_block_forward", "h3_trunk_forward"):
+        assert n in names
+    assert len(names) >= 10
+
+
+def test_library_exports_every_declared_symbol(h3mod):
+    L = h3mod.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert sorted(h3mod.EXPORTS) == _declared()
+
+
+def test_status_strings(h3mod):
+    assert h3mod.h3_status_str(0) == "ok"
+    assert "invalid" in h3mod.h3_status_str(1)
+    assert h3mod.h3_status_str(99) == "unknown status"
+
+
+def _tiny_dims(h3mod):
+    import synth
+
+    from joint_video_audio_block_b300 import runtime as R
+
+    return R.dims_of(synth.TINY)
+
+
+def test_workspace_plan(h3mod):
+    import synth
+
+    d = _tiny_dims(h3mod)
+    n = 72
+    D = synth.TINY
+    a = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    ld_vt = (n + 63) // 64 * 64
+    expect = (a(n * D.head_dim // 2 * 8) + a(n * D.hidden * 2) + a(n * max(3 * D.inner, D.ffn) * 2)
+              + 2 * a(n * D.inner * 2) + a(D.heads * D.head_dim * ld_vt * 2) + a(n * D.inner * 2))
+    assert h3mod.h3_workspace_size(d, n) == expect
+    assert h3mod.h3_workspace_size(d, 0) == 0
+    # grows with rows; invalid dims give 0
+    assert h3mod.h3_workspace_size(d, 1000) > h3mod.h3_workspace_size(d, 72)
+    bad = h3mod.make_dims(100, 4, 64, 512, (8, 12, 12))
+    assert h3mod.h3_workspace_size(bad, 72) == 0
+    bad = h3mod.make_dims(192, 4, 64, 512, (8, 12, 11))  # sections must sum to hd/2
+    assert h3mod.h3_workspace_size(bad, 72) == 0
+
+
+def test_invalid_arguments_rejected_before_launch(h3mod):
+    """Null pointers and inconsistent shapes return H3_EINVAL on the host: no CUDA call runs."""
+    L = h3mod.lib()
+    d = _tiny_dims(h3mod)
+    bw = h3mod.h3_block_w()
+    st = L.h3_block_forward(ctypes.byref(d), ctypes.byref(bw), None, 0, 1, None, None, 72, None, None, None, None, 0,
+                            0, None)
+    assert st == h3mod.H3_EINVAL
+    st = L.h3_trunk_forward(ctypes.byref(d), None, 0, None, 1, None, 72, None, None, None, None, 0, 0, None)
+    assert st == h3mod.H3_EINVAL
+    st = L.h3_modcache_build(ctypes.byref(d), None, 1, 96, None, None, 1, None, None)
+    assert st == h3mod.H3_EINVAL
+    lin = h3mod.h3_linear()
+    st = L.h3_linear_forward(ctypes.byref(lin), 0, None, 0, None, 0, 1, None, None, 0, 0, None, None, 0, None)
+    assert st == h3mod.H3_EINVAL
+    st = L.h3_attention(ctypes.byref(d), None, None, None, 72, None, 72, 0, None)
+    assert st == h3mod.H3_EINVAL

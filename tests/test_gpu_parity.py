@@ -1,0 +1,433 @@
+"""GPU parity: every step of the block through the C ABI against the CPU oracle.
+
+Inputs come from the seeded generator (synth); expected values from oracle/ only.  Float
+tolerances (stated by the task for a block output against the fp32/fp64 oracle):
+relative L2 <= 1e-2 and max-abs <= 5e-2.  Bit-exact checks: modulation-table gathers and
+INT8 group-32 unpacking.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import oracle.h3_oracle as O  # noqa: E402
+import synth  # noqa: E402
+from joint_video_audio_block_b300 import h3, runtime as R  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+REL_L2, MAX_ABS = 1e-2, 5e-2
+
+
+def _err(gpu, ref):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300), float(np.abs(gpu - ref).max())
+
+
+def check(gpu, ref, rel=REL_L2, abs_=MAX_ABS, what=""):
+    r, m = _err(gpu, ref)
+    print(f"{what}: rel_l2={r:.3e} max_abs={m:.3e}")
+    assert r <= rel and m <= abs_, f"{what}: rel_l2={r:.3e} (<= {rel}) max_abs={m:.3e} (<= {abs_})"
+
+
+def sync_ok():
+    torch.cuda.synchronize()
+    st, site = h3.h3_last_device_error(h3.stream_ptr())
+    assert st == h3.H3_OK, f"device error word set: site {site:#x}"
+
+
+class Case:
+    """Seeded inputs of one configuration, on host (bits) and device."""
+
+    def __init__(self, name, n_blocks=1, qk_norm=True):
+        self.cfg = cfg = synth.CONFIGS[name]
+        self.d = cfg.dims
+        self.dims = R.dims_of(cfg.dims)
+        self.n = cfg.layout.n_rows
+        self.x_bits = synth.activations(cfg)
+        self.w_bits = [synth.block_weights(cfg, b, qk_norm=qk_norm) for b in range(n_blocks)]
+        self.tag, self.tidx, self.pos = synth.packed_rows(cfg, step=3)
+        self.temb = synth.temb(cfg)
+        aw = [synth.adaln_weights(cfg, b) for b in range(n_blocks)]
+        self.table64, self.table_bf = O.modcache(self.temb, [a for a, _ in aw], [b for _, b in aw])
+        self.T = self.table_bf.shape[0]
+        self.B = n_blocks
+        # device
+        self.x = R.bf16_from_bits(self.x_bits)
+        self.table = R.bf16_from_bits(O.to_bf16_bits(self.table_bf))
+        self.tag_d = torch.from_numpy(self.tag).cuda()
+        self.tidx_d = torch.from_numpy(self.tidx).cuda()
+        self.pos_d = torch.from_numpy(self.pos).cuda()
+        self.aw = aw
+
+    def table_b(self, b):
+        return self.table_bf[:, b, :]
+
+    def table_ptr(self, b):
+        return self.table.data_ptr() + b * 18 * self.d.hidden * 2
+
+    @property
+    def t_stride(self):
+        return self.B * 18 * self.d.hidden
+
+
+# ----------------------------------------------------------------------------- a0
+
+
+@pytest.mark.parametrize("name,n_blocks", [("tiny", 2), ("block1829", 1)])
+def test_modcache_build(name, n_blocks):
+    c = Case(name, n_blocks)
+    temb_d = torch.from_numpy(c.temb).cuda()
+    aw_d = [(R.bf16_from_bits(w), R.bf16_from_bits(b)) for w, b in c.aw]
+    table = torch.empty(c.T, n_blocks, 18 * c.d.hidden, dtype=torch.bfloat16, device="cuda")
+    h3.h3_modcache_build(c.dims, temb_d.data_ptr(), c.T, c.d.temb_dim, [w.data_ptr() for w, _ in aw_d],
+                         [b.data_ptr() for _, b in aw_d], n_blocks, table.data_ptr(), h3.stream_ptr())
+    sync_ok()
+    got = R.f32_from_bf16(table).astype(np.float64)
+    # fp32 accumulation then one bf16 rounding: within one bf16 ulp of the exact value
+    ulp = np.maximum(np.abs(c.table64), 1e-30)
+    ulp = 2.0 ** (np.floor(np.log2(ulp)) - 7)
+    assert np.all(np.abs(got - c.table64) <= ulp), np.abs(got - c.table64).max()
+    assert np.mean(got == c.table_bf) > 0.99
+
+
+# ----------------------------------------------------------------------------- a1 / a6 + gather
+
+
+@pytest.mark.parametrize("name", ["tiny", "block1829"])
+def test_gather_bit_exact(name):
+    """Constant rows normalise to exactly zero, so xn equals the gathered modulation vector."""
+    c = Case(name)
+    H = c.d.hidden
+    xc = torch.full((c.n, H), 0.375, dtype=torch.bfloat16, device="cuda")
+    xn = torch.empty_like(xc)
+    for m in range(6):
+        h3.h3_adaln_modulate(c.dims, xc.data_ptr(), xn.data_ptr(), c.n, c.table_ptr(0), c.t_stride, m, (m + 1) % 6,
+                             c.tag_d.data_ptr(), c.tidx_d.data_ptr(), h3.stream_ptr())
+        sync_ok()
+        ref = O.modulation(c.table_b(0), c.tag, c.tidx, m, H)
+        np.testing.assert_array_equal(R.f32_from_bf16(xn).astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("name", ["tiny", "block1829", "block12936"])
+def test_adaln_modulate(name):
+    c = Case(name)
+    H = c.d.hidden
+    xn = torch.empty_like(c.x)
+    for ms, mc in ((0, 1), (3, 4)):
+        h3.h3_adaln_modulate(c.dims, c.x.data_ptr(), xn.data_ptr(), c.n, c.table_ptr(0), c.t_stride, ms, mc,
+                             c.tag_d.data_ptr(), c.tidx_d.data_ptr(), h3.stream_ptr())
+        sync_ok()
+        tb = c.table_b(0)
+        ref = O.adaln_modulate(O.widen_bf16(c.x_bits), O.modulation(tb, c.tag, c.tidx, ms, H),
+                               O.modulation(tb, c.tag, c.tidx, mc, H), c.d.ln_eps)
+        check(R.f32_from_bf16(xn), ref, rel=4e-3, abs_=3e-2, what=f"adaln {name} m={ms}")
+
+
+# ----------------------------------------------------------------------------- linears (a2/a5/a7/a8)
+
+
+def _linear_case(M, K, n_out, seed=0):
+    x = synth.normal_bf16(seed, 901, (M, K))
+    w = synth.normal_bf16(seed, 902, (n_out, K), 0.0, 0.02)
+    b = synth.normal_bf16(seed, 903, (n_out,), 0.0, 0.02)
+    return x, w, b
+
+
+@pytest.mark.parametrize("flags", [0, h3.H3_F_UNFUSED])
+@pytest.mark.parametrize("M,K,n_out", [(72, 192, 768), (72, 256, 192), (1829, 5376, 21504), (300, 7168, 5376),
+                                       (1, 64, 256), (129, 96, 512)])
+def test_linear_bias(M, K, n_out, flags):
+    if flags and M * K * n_out > 5e10:
+        pytest.skip("reference kernel too slow at this size")
+    x, w, b = _linear_case(M, K, n_out)
+    xd, wd, bd = R.bf16_from_bits(x), R.bf16_from_bits(w), R.bf16_from_bits(b)
+    y = torch.empty(M, n_out, dtype=torch.bfloat16, device="cuda")
+    h3.h3_linear_forward(h3.make_linear(wd, bd), h3.H3_EPI_BIAS, xd.data_ptr(), K, y.data_ptr(), n_out, M,
+                         flags=flags, stream=h3.stream_ptr())
+    sync_ok()
+    ref = O.linear(O.widen_bf16(x), O.widen_bf16(w), O.widen_bf16(b))
+    check(R.f32_from_bf16(y), ref, rel=4e-3, abs_=3e-2, what=f"linear {M}x{K}x{n_out} f{flags}")
+
+
+@pytest.mark.parametrize("flags", [0, h3.H3_F_UNFUSED])
+@pytest.mark.parametrize("M,K,F", [(72, 192, 512), (1829, 5376, 14336), (200, 5376, 384)])
+def test_linear_swiglu(M, K, F, flags):
+    if flags and M * K * F > 5e10:
+        pytest.skip("reference kernel too slow at this size")
+    x, w, b = _linear_case(M, K, 2 * F, seed=1)
+    xd, wd, bd = R.bf16_from_bits(x), R.bf16_from_bits(w), R.bf16_from_bits(b)
+    y = torch.empty(M, F, dtype=torch.bfloat16, device="cuda")
+    h3.h3_linear_forward(h3.make_linear(wd, bd), h3.H3_EPI_SWIGLU, xd.data_ptr(), K, y.data_ptr(), F, M,
+                         flags=flags, stream=h3.stream_ptr())
+    sync_ok()
+    ref = O.swiglu(O.linear(O.widen_bf16(x), O.widen_bf16(w), O.widen_bf16(b)), F)
+    check(R.f32_from_bf16(y), ref, rel=4e-3, abs_=3e-2, what=f"swiglu {M}x{K}x{F} f{flags}")
+
+
+@pytest.mark.parametrize("flags", [0, h3.H3_F_UNFUSED])
+@pytest.mark.parametrize("name,K", [("tiny", 256), ("block1829", 7168), ("block1829", 14336)])
+def test_linear_gate_residual(name, K, flags):
+    c = Case(name)
+    H = c.d.hidden
+    if flags and c.n * K * H > 5e10:
+        pytest.skip("reference kernel too slow at this size")
+    x, w, b = _linear_case(c.n, K, H, seed=2)
+    xd, wd, bd = R.bf16_from_bits(x), R.bf16_from_bits(w), R.bf16_from_bits(b)
+    res = c.x.clone()
+    for m in (2, 5):
+        y = res.clone()  # in place: y is also the residual
+        h3.h3_linear_forward(h3.make_linear(wd, bd), h3.H3_EPI_GATE_RES, xd.data_ptr(), K, y.data_ptr(), H, c.n,
+                             res=y.data_ptr(), table_b=c.table_ptr(0), t_stride=c.t_stride, m_gate=m,
+                             tag=c.tag_d.data_ptr(), tidx=c.tidx_d.data_ptr(), flags=flags, stream=h3.stream_ptr())
+        sync_ok()
+        gate = O.modulation(c.table_b(0), c.tag, c.tidx, m, H)
+        ref = O.widen_bf16(c.x_bits) + gate * O.linear(O.widen_bf16(x), O.widen_bf16(w), O.widen_bf16(b))
+        check(R.f32_from_bf16(y), ref, what=f"gate-res {name} K={K} m={m} f{flags}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "block1829"])
+def test_gate_gather_bit_exact(name):
+    """x = 0, W = 0, bias = 1, res = 0: the GEMM epilogue writes exactly the gathered gate."""
+    c = Case(name)
+    H = c.d.hidden
+    K = 64
+    xd = torch.zeros(c.n, K, dtype=torch.bfloat16, device="cuda")
+    wd = torch.zeros(H, K, dtype=torch.bfloat16, device="cuda")
+    bd = torch.ones(H, dtype=torch.bfloat16, device="cuda")
+    for m in (2, 5):
+        y = torch.zeros(c.n, H, dtype=torch.bfloat16, device="cuda")
+        h3.h3_linear_forward(h3.make_linear(wd, bd), h3.H3_EPI_GATE_RES, xd.data_ptr(), K, y.data_ptr(), H, c.n,
+                             res=y.data_ptr(), table_b=c.table_ptr(0), t_stride=c.t_stride, m_gate=m,
+                             tag=c.tag_d.data_ptr(), tidx=c.tidx_d.data_ptr(), stream=h3.stream_ptr())
+        sync_ok()
+        np.testing.assert_array_equal(R.f32_from_bf16(y).astype(np.float64),
+                                      O.modulation(c.table_b(0), c.tag, c.tidx, m, H))
+
+
+# ----------------------------------------------------------------------------- a9: INT8 group 32
+
+
+@pytest.mark.parametrize("K,n_out", [(192, 768), (5376, 512), (7168, 256)])
+def test_int8_unpack_bit_exact(K, n_out):
+    """Identity activations make the GEMM output the unpacked weights themselves (one exact
+    product per output), which must equal the oracle's fma + bf16 rounding bit for bit."""
+    w = synth.normal_bf16(3, 904, (n_out, K), 0.0, 0.02)
+    q, s, qb = synth.quantize_int8_g32(w)
+    eye = torch.eye(K, dtype=torch.bfloat16, device="cuda")
+    lin = h3.make_linear(torch.from_numpy(q).cuda(), None, R.bf16_from_bits(s), R.bf16_from_bits(qb))
+    y = torch.empty(K, n_out, dtype=torch.bfloat16, device="cuda")
+    h3.h3_linear_forward(lin, h3.H3_EPI_BIAS, eye.data_ptr(), K, y.data_ptr(), n_out, K, stream=h3.stream_ptr())
+    sync_ok()
+    ref = O.dequant_int8_g32(q, s, qb)
+    np.testing.assert_array_equal(R.bits_from_bf16(y).T, O.to_bf16_bits(ref))
+
+
+@pytest.mark.parametrize("flags", [0, h3.H3_F_UNFUSED])
+@pytest.mark.parametrize("epi", [h3.H3_EPI_BIAS, h3.H3_EPI_SWIGLU])
+def test_int8_linear(epi, flags):
+    M, K, n_out = 300, 5376, 1024
+    x, w, b = _linear_case(M, K, n_out, seed=4)
+    q, s, qb = synth.quantize_int8_g32(w)
+    lin = h3.make_linear(torch.from_numpy(q).cuda(), R.bf16_from_bits(b), R.bf16_from_bits(s), R.bf16_from_bits(qb))
+    n_y = n_out // 2 if epi == h3.H3_EPI_SWIGLU else n_out
+    y = torch.empty(M, n_y, dtype=torch.bfloat16, device="cuda")
+    h3.h3_linear_forward(lin, epi, R.bf16_from_bits(x).data_ptr(), K, y.data_ptr(), n_y, M, flags=flags,
+                         stream=h3.stream_ptr())
+    sync_ok()
+    ref = O.linear(O.widen_bf16(x), O.dequant_int8_g32(q, s, qb), O.widen_bf16(b))
+    if epi == h3.H3_EPI_SWIGLU:
+        ref = O.swiglu(ref, n_y)
+    check(R.f32_from_bf16(y), ref, rel=4e-3, abs_=3e-2, what=f"int8 epi{epi} f{flags}")
+
+
+# ----------------------------------------------------------------------------- a3 / a4
+
+
+def _qkv_case(c, seed=5):
+    return synth.normal_bf16(seed, 905, (c.n, 3 * c.d.inner), 0.0, 1.5)
+
+
+@pytest.mark.parametrize("name,qk", [("tiny", True), ("tiny", False), ("block1829", True)])
+def test_qknorm_rope(name, qk):
+    c = Case(name, qk_norm=qk)
+    d = c.d
+    qkv = _qkv_case(c)
+    ld_vt = (c.n + 63) // 64 * 64
+    q = torch.empty(d.heads, c.n, d.head_dim, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty_like(q)
+    vt = torch.zeros(d.heads, d.head_dim, ld_vt, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(c.n * d.head_dim * 4, dtype=torch.uint8, device="cuda")
+    wt = R.upload_block(c.w_bits[0])
+    h3.h3_qknorm_rope(c.dims, R.bf16_from_bits(qkv).data_ptr(), c.pos_d.data_ptr(), h3.ptr(wt.get("qnorm")),
+                      h3.ptr(wt.get("knorm")), q.data_ptr(), k.data_ptr(), vt.data_ptr(), ld_vt, c.n, ws.data_ptr(),
+                      ws.numel(), h3.stream_ptr())
+    sync_ok()
+    rq, rk, rv = O.split_qkv(O.widen_bf16(qkv), d.heads, d.head_dim)
+    if qk:
+        rq = O.rms_norm(rq, O.widen_bf16(c.w_bits[0]["qnorm"]), d.qk_eps)
+        rk = O.rms_norm(rk, O.widen_bf16(c.w_bits[0]["knorm"]), d.qk_eps)
+    rq = O.rope(rq, c.pos, d.head_dim, d.rope_theta, d.rope_sections)
+    rk = O.rope(rk, c.pos, d.head_dim, d.rope_theta, d.rope_sections)
+    check(R.f32_from_bf16(q).transpose(1, 0, 2), rq, rel=4e-3, abs_=3e-2, what="q")
+    check(R.f32_from_bf16(k).transpose(1, 0, 2), rk, rel=4e-3, abs_=3e-2, what="k")
+    got_v = R.f32_from_bf16(vt)[:, :, : c.n].transpose(2, 0, 1)
+    np.testing.assert_array_equal(got_v, rv)  # v is moved, not computed
+    assert np.all(R.f32_from_bf16(vt)[:, :, c.n:] == 0)
+
+
+def _attn_inputs(n, nh, hd, seed):
+    q = synth.normal_bf16(seed, 906, (nh, n, hd))
+    k = synth.normal_bf16(seed, 907, (nh, n, hd))
+    v = synth.normal_bf16(seed, 908, (nh, n, hd))
+    return q, k, v
+
+
+@pytest.mark.parametrize("flags", [0, h3.H3_F_UNFUSED])
+@pytest.mark.parametrize("n,nh,hd,rows", [(72, 4, 64, None), (1, 2, 128, None), (130, 2, 128, None),
+                                          (300, 3, 128, None), (1829, 56, 128, 200), (12936, 8, 128, 96)])
+def test_attention(n, nh, hd, rows, flags):
+    if flags and n > 5000:
+        pytest.skip("reference kernel too slow at this size")
+    q, k, v = _attn_inputs(n, nh, hd, seed=n)
+    ld_vt = (n + 63) // 64 * 64
+    vt = np.zeros((nh, hd, ld_vt), np.uint16)
+    vt[:, :, :n] = v.transpose(0, 2, 1)
+    o = torch.empty(n, nh * hd, dtype=torch.bfloat16, device="cuda")
+    dims = h3.make_dims(nh * hd if (nh * hd) % 64 == 0 else 64, nh, hd, 128,
+                        (hd // 8, 3 * hd // 16, 3 * hd // 16))
+    h3.h3_attention(dims, R.bf16_from_bits(q).data_ptr(), R.bf16_from_bits(k).data_ptr(),
+                    R.bf16_from_bits(vt).data_ptr(), ld_vt, o.data_ptr(), n, flags, h3.stream_ptr())
+    sync_ok()
+    sel = np.arange(n) if rows is None else np.random.default_rng(n).choice(n, rows, replace=False)
+    t = lambda a: O.widen_bf16(a).transpose(1, 0, 2)  # noqa: E731
+    ref = O.attention(t(q), t(k), t(v), rows=sel).reshape(len(sel), nh * hd)
+    check(R.f32_from_bf16(o)[sel], ref, rel=1e-2, abs_=2e-2, what=f"attention n={n} f{flags}")
+
+
+# ----------------------------------------------------------------------------- block / trunk
+
+
+def _run_block(c, wt, x_in, x_out, flags=0, b=0):
+    ws = R.workspace(c.dims, c.n)
+    bw = h3.make_block_w(wt)
+    h3.h3_block_forward(c.dims, bw, c.table_ptr(b), c.t_stride, c.T, x_in.data_ptr(), x_out.data_ptr(), c.n,
+                        c.tag_d.data_ptr(), c.tidx_d.data_ptr(), c.pos_d.data_ptr(), ws.data_ptr(), ws.numel(), flags,
+                        h3.stream_ptr())
+    sync_ok()
+
+
+@pytest.mark.parametrize("flags", [0, h3.H3_F_UNFUSED, h3.H3_F_NO_QKNORM])
+def test_block_tiny(flags):
+    c = Case("tiny")
+    wt = R.upload_block(c.w_bits[0])
+    out = torch.empty_like(c.x)
+    _run_block(c, wt, c.x, out, flags)
+    w = dict(c.w_bits[0])
+    if flags & h3.H3_F_NO_QKNORM:
+        w.pop("qnorm"), w.pop("knorm")
+    ref = O.block_forward(c.x_bits, w, c.table_b(0), c.tag, c.tidx, c.pos, c.d)
+    check(R.f32_from_bf16(out), ref, what=f"block tiny f{flags}")
+
+
+def test_block_in_place_matches_out_of_place():
+    c = Case("tiny")
+    wt = R.upload_block(c.w_bits[0])
+    out = torch.empty_like(c.x)
+    _run_block(c, wt, c.x, out)
+    xi = c.x.clone()
+    _run_block(c, wt, xi, xi)
+    assert torch.equal(out, xi)
+
+
+def test_block_zero_gates_identity():
+    c = Case("tiny")
+    H = c.d.hidden
+    tb = c.table.clone().view(c.T, c.B, 18, H)
+    tb[:, :, [2, 5, 8, 11, 14, 17], :] = 0
+    c.table = tb.view(c.T, c.B, 18 * H)
+    wt = R.upload_block(c.w_bits[0])
+    out = torch.empty_like(c.x)
+    _run_block(c, wt, c.x, out)
+    assert torch.equal(out, c.x)
+
+
+def test_block1829_full():
+    c = Case("block1829")
+    wt = R.upload_block(c.w_bits[0])
+    out = torch.empty_like(c.x)
+    _run_block(c, wt, c.x, out)
+    ref = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d)
+    check(R.f32_from_bf16(out), ref, what="block 1829 rows")
+
+
+@pytest.mark.parametrize("name", ["block12936", "block12936_int8"])
+def test_block12936_sampled(name):
+    c = Case(name)
+    int8 = c.cfg.int8
+    wt = R.upload_block(c.w_bits[0], int8=int8, quantize=synth.quantize_int8_g32)
+    out = torch.empty_like(c.x)
+    _run_block(c, wt, c.x, out)
+    rows = np.random.default_rng(7).choice(c.n, 256, replace=False)
+    deq = None
+    if int8:
+        deq = {n: O.dequant_int8_g32(*synth.quantize_int8_g32(c.w_bits[0][n])) for n in ("wqkv", "wo", "w1", "w2")}
+    ref = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows, dequant=deq)
+    check(R.f32_from_bf16(out)[rows], ref, what=f"{name} sampled")
+    if int8:
+        # report the distance to the bf16 masters (not a tolerance: quantisation error)
+        ref_m = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows)
+        r, m = _err(R.f32_from_bf16(out)[rows], ref_m)
+        print(f"int8 block vs bf16 masters: rel_l2={r:.3e} max_abs={m:.3e}")
+
+
+def test_trunk_equals_block_sequence():
+    c = Case("block1829", n_blocks=3)
+    wts = [R.upload_block(w) for w in c.w_bits]
+    ws = R.workspace(c.dims, c.n)
+    x_seq = c.x.clone()
+    for b in range(3):
+        _run_block(c, wts[b], x_seq, x_seq, b=b)
+    x_tr = c.x.clone()
+    h3.h3_trunk_forward(c.dims, [h3.make_block_w(w) for w in wts], 3, c.table.data_ptr(), c.T, x_tr.data_ptr(), c.n,
+                        c.tag_d.data_ptr(), c.tidx_d.data_ptr(), c.pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0,
+                        h3.stream_ptr())
+    sync_ok()
+    assert torch.equal(x_tr, x_seq)
+    ref = O.trunk_forward(c.x_bits, c.w_bits, c.table_bf, c.tag, c.tidx, c.pos, c.d)
+    ref_e = O.trunk_forward(c.x_bits, c.w_bits, c.table_bf, c.tag, c.tidx, c.pos, c.d, emulate_bf16=True)
+    r, m = _err(R.f32_from_bf16(x_tr), ref)
+    r2, m2 = _err(R.f32_from_bf16(x_tr), ref_e)
+    print(f"trunk 3x1829: vs exact rel_l2={r:.3e} max_abs={m:.3e}; vs bf16-storage oracle rel_l2={r2:.3e} max_abs={m2:.3e}")
+    check(R.f32_from_bf16(x_tr), ref, rel=REL_L2, abs_=0.15, what="trunk 3 blocks")
+
+
+# ----------------------------------------------------------------------------- edges / errors
+
+
+def test_zero_rows_and_bad_arguments():
+    c = Case("tiny")
+    wt = R.upload_block(c.w_bits[0])
+    ws = R.workspace(c.dims, c.n)
+    bw = h3.make_block_w(wt)
+    args = [c.dims, bw, c.table_ptr(0), c.t_stride, c.T, c.x.data_ptr(), c.x.data_ptr(), 0, c.tag_d.data_ptr(),
+            c.tidx_d.data_ptr(), c.pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0, h3.stream_ptr()]
+    h3.h3_block_forward(*args)  # zero rows: nothing to do
+    bad = list(args)
+    bad[7] = c.n
+    bad[12] = 16  # workspace too small
+    with pytest.raises(h3.H3Error) as e:
+        h3.h3_block_forward(*bad)
+    assert e.value.status == h3.H3_EINVAL
+    # out-of-range tag caught by the index check
+    tag_bad = c.tag_d.clone()
+    tag_bad[5] = 7
+    bad = list(args)
+    bad[7], bad[8], bad[13] = c.n, tag_bad.data_ptr(), h3.H3_F_CHECK_INDEX
+    with pytest.raises(h3.H3Error):
+        h3.h3_block_forward(*bad)
+    sync_ok()
