@@ -171,6 +171,7 @@ def make_linear(w, bias=None, scale=None, qbias=None):
     lw.fmt = H3_W_INT8_G32 if w.dtype == torch.uint8 else H3_W_BF16
     lw.w, lw.scale, lw.qbias, lw.bias = ptr(w), ptr(scale), ptr(qbias), ptr(bias)
     lw.n_out, lw.k = int(w.shape[0]), int(w.shape[1])
+    lw._refs = (w, bias, scale, qbias)  # the struct holds raw pointers: keep the tensors alive with it
     return lw
 
 
@@ -181,4 +182,5 @@ def make_block_w(t: dict):
         bname = "b" + lname[1:]
         setattr(bw, name, make_linear(t[lname], t.get(bname), t.get(lname + "_scale"), t.get(lname + "_qbias")))
     bw.q_norm, bw.k_norm = ptr(t.get("qnorm")), ptr(t.get("knorm"))
+    bw._refs = dict(t)  # keep every tensor the struct points at alive with it
     return bw
