@@ -51,6 +51,7 @@ struct GemmParams {
   const bf16* wscale;  // INT8: [rows, K/32]
   const bf16* wqbias;
   int groups;          // K / 32
+  int w_rows;          // rows of W (codes beyond it are TMA zero fill; their scales are not read)
   unsigned* err;
 };
 
@@ -194,7 +195,7 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* sq, uint8_t* sb, co
     const int n = (t >> 2) + 32 * i;                  // row within the 256-row tile
     const int grow = (n < 128) ? brow0 + n : brow1 + (n - 128);
     float sc = 0.f, qb = 0.f;
-    if (g < p.groups) {
+    if (g < p.groups && grow < p.w_rows) {
       const size_t gi = static_cast<size_t>(grow) * p.groups + g;
       sc = bf2f(p.wscale[gi]);
       qb = bf2f(p.wqbias[gi]);
@@ -455,6 +456,7 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
   p.groups = a.K / 32;
   p.err = a.err;
   const int w_rows = sw ? 2 * a.n_y : a.n_y;
+  p.w_rows = w_rows;
 
   CUtensorMap ta, tb;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, a.K, a.M, static_cast<uint64_t>(a.lda) * 2, G_BK, G_BM,
