@@ -162,6 +162,26 @@ h3_status h3_qknorm_rope(const h3_dims* dims, const void* qkv, const float* pos,
 h3_status h3_attention(const h3_dims* dims, const void* q, const void* k, const void* vt, int ld_vt, void* o,
                        int n_rows, unsigned flags, void* stream);
 
+/* h3_qknorm_rope without a caller-supplied workspace.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory at the call site (an
+ * embedder whose device memory belongs to a pool or allocator it cannot reach there, or a
+ * latency-critical loop that must not take cudaMalloc's implicit device synchronisation).
+ * It computes exactly what h3_qknorm_rope computes, with the same arguments minus
+ * workspace/ws_bytes, and allocates nothing: the cos/sin scratch is a fixed device array
+ * inside the library (16 MiB, held on every device that loads the library until the process
+ * exits) holding up to H3_QKROPE_STATIC_MAX_PAIRS (row, frequency) pairs.
+ *   n_rows * head_dim / 2 > H3_QKROPE_STATIC_MAX_PAIRS (32768 rows at head_dim 128, 65536 at
+ *   64) returns H3_EINVAL before any launch; so do the argument errors of h3_qknorm_rope.
+ * The first call on a device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture.  Every call shares the
+ * array: calls whose GPU work overlaps (different streams without ordering) race on it and
+ * must be serialised by the caller.  Each call rewrites the part it reads, so the array needs
+ * no clearing. */
+#define H3_QKROPE_STATIC_MAX_PAIRS (1 << 21)
+h3_status h3_qknorm_rope_static(const h3_dims* dims, const void* qkv, const float* pos, const void* q_norm,
+                                const void* k_norm, void* q_out, void* k_out, void* vt_out, int ld_vt, int n_rows,
+                                void* stream);
+
 /* Synchronises `stream`, then reads and clears the device error word.  Returns H3_OK, or
  * H3_ETIMEOUT when a bounded device wait ran out since the last call (*site, if not NULL,
  * receives the site code), or H3_ECUDA if the stream reports a CUDA error. */

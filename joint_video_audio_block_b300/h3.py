@@ -22,8 +22,12 @@ H3_EPI_BIAS, H3_EPI_SWIGLU, H3_EPI_GATE_RES = 0, 1, 2
 # every symbol include/h3.h declares
 EXPORTS = (
     "h3_workspace_size", "h3_modcache_build", "h3_block_forward", "h3_trunk_forward", "h3_adaln_modulate",
-    "h3_linear_forward", "h3_qknorm_rope", "h3_attention", "h3_last_device_error", "h3_status_str",
+    "h3_linear_forward", "h3_qknorm_rope", "h3_qknorm_rope_static", "h3_attention", "h3_last_device_error",
+    "h3_status_str",
 )
+
+# largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
+H3_QKROPE_STATIC_MAX_PAIRS = 1 << 21
 
 
 class H3Error(RuntimeError):
@@ -67,6 +71,7 @@ def lib():
             "h3_adaln_modulate": (i32, [D, vp, vp, i32, vp, i64, i32, i32, vp, vp, vp]),
             "h3_linear_forward": (i32, [LW, i32, vp, i32, vp, i32, i32, vp, vp, i64, i32, vp, vp, u32, vp]),
             "h3_qknorm_rope": (i32, [D, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, vp]),
+            "h3_qknorm_rope_static": (i32, [D, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp]),
             "h3_attention": (i32, [D, vp, vp, vp, i32, vp, i32, u32, vp]),
             "h3_last_device_error": (i32, [vp, ctypes.POINTER(u32)]),
             "h3_status_str": (ctypes.c_char_p, [i32]),
@@ -128,6 +133,14 @@ def h3_linear_forward(lin, epilogue, x, lda, y, ldy, n_rows, res=None, table_b=N
 def h3_qknorm_rope(dims, qkv, pos, q_norm, k_norm, q_out, k_out, vt_out, ld_vt, n_rows, workspace, ws_bytes, stream):
     _check(lib().h3_qknorm_rope(ctypes.byref(dims), qkv, pos, q_norm, k_norm, q_out, k_out, vt_out, ld_vt, n_rows,
                                 workspace, ws_bytes, stream), "h3_qknorm_rope")
+
+
+def h3_qknorm_rope_static(dims, qkv, pos, q_norm, k_norm, q_out, k_out, vt_out, ld_vt, n_rows, stream):
+    """h3_qknorm_rope with the library's fixed scratch array instead of a workspace (for callers
+    that cannot allocate device memory at the call site); n_rows * head_dim / 2 must not exceed
+    H3_QKROPE_STATIC_MAX_PAIRS."""
+    _check(lib().h3_qknorm_rope_static(ctypes.byref(dims), qkv, pos, q_norm, k_norm, q_out, k_out, vt_out, ld_vt,
+                                       n_rows, stream), "h3_qknorm_rope_static")
 
 
 def h3_attention(dims, q, k, vt, ld_vt, o, n_rows, flags, stream):
