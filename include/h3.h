@@ -94,7 +94,7 @@ size_t h3_workspace_size(const h3_dims* dims, int n_rows);
 /* a0 -- ModulationCache build ("minimax-h3-mlx" README, "AdaLN precompute").
  *   table[t][b][j] = bf16( sum_k adaln_w[b][j][k] * temb[t][k] + adaln_b[b][j] ),
  * fp32 accumulation, j < 18*H.
- * temb: device f32 [T, Dt]; adaln_w: HOST array of n_blocks device pointers to bf16 [18H, Dt];
+ * temb: device f32 [T, Dt]; adaln_w: HOST array of n_blocks device pointers (16-byte aligned) to bf16 [18H, Dt];
  * adaln_b: HOST array of n_blocks device pointers to bf16 [18H] (array or entries may be NULL);
  * table: device bf16 [T][n_blocks][18H], written.  Dt % 8 == 0. */
 h3_status h3_modcache_build(const h3_dims* dims, const float* temb, int T, int Dt, const void* const* adaln_w,
@@ -131,7 +131,7 @@ h3_status h3_adaln_modulate(const h3_dims* dims, const void* x, void* xn, int n_
 
 /* epilogues of h3_linear_forward */
 #define H3_EPI_BIAS 0      /* y = x W^T + b                                                   */
-#define H3_EPI_SWIGLU 1    /* y = silu(g) * v, [g | v] = x W^T + b, W has 2*n_out rows (gate first) */
+#define H3_EPI_SWIGLU 1    /* y = silu(g) * v, [g | v] = x W^T + b; W has 2*n_y rows (gate rows first) */
 #define H3_EPI_GATE_RES 2  /* y = res + gate(r) * (x W^T + b), gate from the modulation table */
 
 /* a2 / a5 / a7 / a8 / a9 -- one linear with a fused epilogue on the tcgen05 tensor cores.

@@ -242,7 +242,7 @@ h3_status h3_modcache_build(const h3_dims* dims, const float* temb, int T, int D
   const long long t_stride = static_cast<long long>(n_blocks) * n_out;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   for (int b = 0; b < n_blocks; ++b) {
-    if (!adaln_w[b]) return H3_EINVAL;
+    if (!adaln_w[b] || !aligned16(adaln_w[b])) return H3_EINVAL;
     const bf16* bias = adaln_b ? static_cast<const bf16*>(adaln_b[b]) : nullptr;
     cudaError_t e = launch_modcache(temb, T, Dt, static_cast<const bf16*>(adaln_w[b]), bias, n_out,
                                     static_cast<bf16*>(table) + static_cast<long long>(b) * n_out, t_stride, st);

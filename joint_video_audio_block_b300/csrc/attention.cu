@@ -4,18 +4,23 @@
 // packed sequence (no cross-attention, no mask); "Performance": it is flash-style (the score
 // matrix is never materialised) and dominates the work at realistic lengths.
 //
-// One CTA = one head x 128 query rows.  Roles:
-//   warp 0      TMA producer: Q once, then K and V^T tiles of 128 keys (2-stage ring)
-//   warp 1      TMEM allocator + single-thread MMA issuer:
-//                 S_j  = Q K_j^T        -> TMEM (two 128-column buffers, so S_{j+1} runs
-//                                          while the softmax reads S_j)
-//                 O   += P_j V_j        -> TMEM (128 columns), A = P from shared memory,
-//                                          B = V^T tile (keys contiguous: K-major)
-//   warps 2..5  softmax: one thread per query row (its TMEM lane), online max / sum in fp32,
-//               P rounded to bf16 into the 128-byte-swizzled A-operand layout; O is rescaled
-//               in TMEM only when the running max grew by more than 2^8 (the stale max keeps
-//               every exponent <= 2^8, and l and O share it, so the result is unchanged).
-// Keys beyond n_rows in the last tile get a score of -inf (TMA fills them with zeros).
+// One CTA = one head x two 128-row query tiles (A and B) that share every K/V tile, so the
+// tensor core always has the other tile's work while one tile's softmax runs:
+//   warp 0       TMA producer: Q_A, Q_B once, then K_j and V_j^T tiles of 128 keys (ring)
+//   warp 1       TMEM allocator + single-thread MMA issuer, per key tile j:
+//                  O_A += P_A(j) V_j   (A operand P from TMEM)      S_A(j+1) = Q_A K_{j+1}^T
+//                  O_B += P_B(j) V_j                                S_B(j+1) = Q_B K_{j+1}^T
+//   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B: one thread per query row
+//                (its TMEM lane); the row of S is read with tcgen05.ld, the online max / sum
+//                kept in fp32, and P rounded to bf16 written back over the front half of the
+//                same S columns with tcgen05.st, where the P.V MMA reads it.
+// TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256.., O_B 256+HD.. (fp32).  tcgen05.mma
+// from one thread complete in issue order, so S_X(j+1) (issued after PV_X(j)) may overwrite
+// P_X(j), and the completion of S_X(j+1) also means PV_X(j) is done: the softmax may then
+// rescale O_X in TMEM before releasing P_X(j+1).  O is rescaled only when the running max grew
+// by more than 2^8 (the stale max bounds every exponent by 2^8 and l and O share it, so the
+// normalised result is unchanged).  Keys beyond n_rows in the last tile get a score of -inf
+// (TMA fills them with zeros).
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -24,23 +29,74 @@ namespace h3 {
 
 constexpr int AT_BM = 128, AT_BN = 128;
 constexpr int AT_ATOM = 128 * 128;            // one 128-row x 128-byte swizzle atom
-constexpr int AT_THREADS = 192;
+constexpr int AT_THREADS = 384;
+// Register split (setmaxnreg): the kernel launches at AT_LAUNCH_REGS per thread (checked on the
+// host before every launch); warps 0..3 then give back down to AT_REGS_CTRL and the eight
+// softmax warps take AT_REGS_SOFTMAX.  128 * 72 + 256 * 216 = 384 * 168, so the increase is
+// always covered by the block's own launch allocation.
+constexpr int AT_LAUNCH_REGS = 168, AT_REGS_CTRL = 72, AT_REGS_SOFTMAX = 216;
+static_assert(128 * AT_REGS_CTRL + 256 * AT_REGS_SOFTMAX <= AT_THREADS * AT_LAUNCH_REGS, "register split");
 constexpr float AT_RESCALE_THRESHOLD = 8.0f;  // log2 units
 
-// Shared-memory plan for head_dim HD: Q and K tiles are 128 rows x HD (HD/64 atoms along d),
-// V^T tiles are HD rows x 128 keys (2 atoms along keys, HD*128 bytes each), P is 128 x 128.
+// Shared-memory plan for head_dim HD: each Q and K tile is 128 rows x HD (HD/64 atoms along
+// d); each V^T tile is HD rows x 128 keys (2 atoms along keys, HD*128 bytes each).
 template <int HD>
 struct AtCfg {
+  static constexpr int STAGES = HD == 64 ? 4 : 2;
   static constexpr int QK_TILE = 128 * HD * 2;
   static constexpr int V_ATOM = HD * 128;
   static constexpr int V_TILE = 2 * V_ATOM;
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = QK_TILE;               // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * QK_TILE;   // 2 stages
-  static constexpr int P_OFF = V_OFF + 2 * V_TILE;
-  static constexpr int BAR_OFF = P_OFF + 2 * AT_ATOM;
+  static constexpr int Q_OFF = 0;                         // Q_A, Q_B
+  static constexpr int K_OFF = 2 * QK_TILE;               // STAGES
+  static constexpr int V_OFF = K_OFF + STAGES * QK_TILE;  // STAGES
+  static constexpr int BAR_OFF = V_OFF + STAGES * V_TILE;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;
 };
+
+// softmax arithmetic helpers: 3-input max, the SFU base-2 exponential (flushes results below
+// 2^-126 to zero, which only drops probabilities that bf16 P cannot carry anyway), and
+// paired fp32 FMA / add on two lanes of a 64-bit register
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint64_t pack_u32x2(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return pack_u32x2(__float_as_uint(lo), __float_as_uint(hi));
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread (A: 128 lanes x K/2 columns of bf16 pairs)
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 template <int HD>
 __global__ void __launch_bounds__(AT_THREADS, 1)
@@ -48,32 +104,35 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ o, int n_rows, int nh,
                         float scale_log2, unsigned* err) {
   using C = AtCfg<HD>;
+  constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   const uint32_t b_q = smem_u32(bars);
-  const uint32_t b_kfull = b_q + 8;        // [2]
-  const uint32_t b_vfull = b_kfull + 16;   // [2]
-  const uint32_t b_kvempty = b_vfull + 16; // [2]
-  const uint32_t b_sfull = b_kvempty + 16; // [2]
-  const uint32_t b_pfull = b_sfull + 16;
-  const uint32_t b_odone = b_pfull + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  const uint32_t b_kfull = b_q + 8;               // [ST]
+  const uint32_t b_vfull = b_kfull + 8 * ST;      // [ST]
+  const uint32_t b_kvempty = b_vfull + 8 * ST;    // [ST]
+  const uint32_t b_sfull = b_kvempty + 8 * ST;    // [2] (tile A, tile B)
+  const uint32_t b_pfull = b_sfull + 16;          // [2]
+  const uint32_t b_odone = b_pfull + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + 3 * ST + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
-  const int q0 = blockIdx.x * AT_BM;
+  const int q0 = blockIdx.x * 2 * AT_BM;
   const int nt = cdiv(n_rows, AT_BN);
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(b_kfull + 8 * s, 1);
       mbar_init(b_vfull + 8 * s, 1);
       mbar_init(b_kvempty + 8 * s, 1);
-      mbar_init(b_sfull + 8 * s, 1);
     }
-    mbar_init(b_pfull, 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(b_sfull + 8 * x, 1);
+      mbar_init(b_pfull + 8 * x, 4);
+    }
     mbar_init(b_odone, 1);
     fence_barrier_init();
   }
@@ -90,20 +149,22 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t t_s0 = tmem, t_o = tmem + 256;
+
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(AT_REGS_CTRL));
 
   const uint32_t sQ = smem_u32(smem + C::Q_OFF);
   const uint32_t sK = smem_u32(smem + C::K_OFF);
   const uint32_t sV = smem_u32(smem + C::V_OFF);
-  const uint32_t sP = smem_u32(smem + C::P_OFF);
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(b_q, C::QK_TILE);
-      for (int a = 0; a < HD / 64; ++a) tma_load_3d(sQ + a * AT_ATOM, &tmQ, b_q, 64 * a, q0, h);
+      mbar_arrive_expect_tx(b_q, 2 * C::QK_TILE);
+      for (int x = 0; x < 2; ++x)
+        for (int a = 0; a < HD / 64; ++a)
+          tma_load_3d(sQ + x * C::QK_TILE + a * AT_ATOM, &tmQ, b_q, 64 * a, q0 + x * AT_BM, h);
       for (int j = 0; j < nt; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(b_kvempty + 8 * s, ((j >> 1) & 1) ^ 1, err, kErrAttnProducer)) break;
+        const int s = j % ST;
+        if (!mbar_wait(b_kvempty + 8 * s, ((j / ST) & 1) ^ 1, err, kErrAttnProducer)) break;
         const uint32_t kd = sK + s * C::QK_TILE, vd = sV + s * C::V_TILE;
         mbar_arrive_expect_tx(b_kfull + 8 * s, C::QK_TILE);
         for (int a = 0; a < HD / 64; ++a) tma_load_3d(kd + a * AT_ATOM, &tmK, b_kfull + 8 * s, 64 * a, j * AT_BN, h);
@@ -116,138 +177,144 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD);
-      bool ok = mbar_wait(b_q, 0, err, kErrAttnMma);
-      // S_0
-      if (ok) ok = mbar_wait(b_kfull, 0, err, kErrAttnMma);
-      if (ok) {
-        tc_fence_after();
+      auto issue_s = [&](int x, int j) {  // S_x(j) = Q_x K_j^T
+        const uint32_t kb = sK + (j % ST) * C::QK_TILE, qb = sQ + x * C::QK_TILE;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * AT_ATOM + (kk & 3) * 32;
-          umma_bf16_ss(t_s0, sdesc_k_sw128(sQ + off), sdesc_k_sw128(sK + off), idesc_s, kk != 0);
+          umma_bf16_ss(tmem + x * 128, sdesc_k_sw128(qb + off), sdesc_k_sw128(kb + off), idesc_s, kk != 0);
         }
-        umma_commit(b_sfull);
+        umma_commit(b_sfull + 8 * x);
+      };
+      auto issue_pv = [&](int x, int j) {  // O_x += P_x(j) V_j
+        const uint32_t vb = sV + (j % ST) * C::V_TILE;
+#pragma unroll
+        for (int kk = 0; kk < AT_BN / 16; ++kk)
+          umma_bf16_ts(tmem + 256 + x * HD, tmem + x * 128 + kk * 8,
+                       sdesc_k_sw128(vb + (kk >> 2) * C::V_ATOM + (kk & 3) * 32), idesc_o, (j | kk) != 0);
+      };
+      bool ok = mbar_wait(b_q, 0, err, kErrAttnMma) && mbar_wait(b_kfull, 0, err, kErrAttnMma);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
       }
       for (int j = 0; ok && j < nt; ++j) {
-        const int s = j & 1;
-        if (j + 1 < nt) {
-          const int s1 = (j + 1) & 1;
-          if (!mbar_wait(b_kfull + 8 * s1, ((j + 1) >> 1) & 1, err, kErrAttnMma)) break;
-          tc_fence_after();
-          const uint32_t kb = sK + s1 * C::QK_TILE;
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * AT_ATOM + (kk & 3) * 32;
-            umma_bf16_ss(t_s0 + s1 * 128, sdesc_k_sw128(sQ + off), sdesc_k_sw128(kb + off), idesc_s, kk != 0);
-          }
-          umma_commit(b_sfull + 8 * s1);
-        }
-        if (!mbar_wait(b_pfull, j & 1, err, kErrAttnMma)) break;
-        if (!mbar_wait(b_vfull + 8 * s, (j >> 1) & 1, err, kErrAttnMma)) break;
+        const int s = j % ST;
+        const uint32_t par = (j / ST) & 1;
+        const bool more = j + 1 < nt;
+        // tile A: P_A(j) V_j, then S_A(j+1)
+        if (!mbar_wait(b_pfull, j & 1, err, kErrAttnMma) || !mbar_wait(b_vfull + 8 * s, par, err, kErrAttnMma)) break;
         tc_fence_after();
-        const uint32_t vb = sV + s * C::V_TILE;
-#pragma unroll
-        for (int kk = 0; kk < AT_BN / 16; ++kk) {
-          const uint32_t inner = (kk & 3) * 32;
-          umma_bf16_ss(t_o, sdesc_k_sw128(sP + (kk >> 2) * AT_ATOM + inner),
-                       sdesc_k_sw128(vb + (kk >> 2) * C::V_ATOM + inner), idesc_o, (j | kk) != 0);
+        issue_pv(0, j);
+        if (more) {
+          if (!mbar_wait(b_kfull + 8 * ((j + 1) % ST), ((j + 1) / ST) & 1, err, kErrAttnMma)) break;
+          tc_fence_after();
+          issue_s(0, j + 1);
         }
+        // tile B: P_B(j) V_j, release K_j / V_j, then S_B(j+1)
+        if (!mbar_wait(b_pfull + 8, j & 1, err, kErrAttnMma)) break;
+        tc_fence_after();
+        issue_pv(1, j);
         umma_commit(b_kvempty + 8 * s);
-        umma_commit(b_odone);
+        if (more) issue_s(1, j + 1);
       }
+      if (ok) umma_commit(b_odone);
     }
-  } else {
-    // softmax warps 2..5: TMEM lane quadrant = warp % 4, one query row per thread
+  } else if (warp >= 4) {
+    // softmax warps: tile x = 0 (warps 4..7) or 1 (warps 8..11); TMEM lane quadrant = warp % 4
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_REGS_SOFTMAX));
+    const int x = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;  // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + x * 128;
+    const uint32_t t_o = tmem + lane_off + 256 + x * HD;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    uint8_t* prow = smem + C::P_OFF + r * 128;
     for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(b_sfull + 8 * sb, (j >> 1) & 1, err, kErrAttnSoftmax)) {
+      if (!mbar_wait(b_sfull + 8 * x, j & 1, err, kErrAttnSoftmax)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float sv[128];
+      uint32_t sv[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(t_s0 + sb * 128 + lane_off + c * 32, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(u[i]) * scale_log2;
+        uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]);
+        tmem_ld32(t_s + c * 32, chunk);
       }
+      tmem_wait_ld();
       const int valid = n_rows - j * AT_BN;  // keys of this tile that exist
-      float mt = -INFINITY;
+      if (valid < AT_BN) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        if (i >= valid) sv[i] = -INFINITY;
-        mt = fmaxf(mt, sv[i]);
+        for (int i = 0; i < 128; ++i)
+          if (i >= valid) sv[i] = __float_as_uint(-INFINITY);
       }
+      // row max with 3-input max (tree of 43 + 1 instructions for 128 values)
+      float mq[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float m = __uint_as_float(sv[32 * c]);
+#pragma unroll
+        for (int i = 1; i < 31; i += 2) m = fmax3f(m, __uint_as_float(sv[32 * c + i]), __uint_as_float(sv[32 * c + i + 1]));
+        mq[c] = fmaxf(m, __uint_as_float(sv[32 * c + 31]));
+      }
+      const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * scale_log2;
       float alpha = 1.f;
       bool rescale = false;
       if (j == 0) {
         m_used = mt;
       } else if (mt > m_used + AT_RESCALE_THRESHOLD) {
-        alpha = exp2f(m_used - mt);
+        alpha = ex2f(m_used - mt);
         m_used = mt;
         rescale = true;
       }
-      float rs = 0.f;
-      uint32_t pk[64];
+      // p = 2^(s * scale - m): paired f32x2 FMA and add, ex2 on the SFU, bf16x2 pack
+      const uint64_t c2 = pack_f32x2(scale_log2, scale_log2);
+      const uint64_t nm2 = pack_f32x2(-m_used, -m_used);
+      uint64_t rs2 = pack_f32x2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = exp2f(sv[2 * i] - m_used);
-        const float p1 = exp2f(sv[2 * i + 1] - m_used);
-        rs += p0 + p1;
-        pk[i] = pack_bf16x2(p0, p1);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t e2 = fma_f32x2(pack_u32x2(sv[32 * c + 2 * i], sv[32 * c + 2 * i + 1]), c2, nm2);
+          const float p0 = ex2f(lo_f32(e2)), p1 = ex2f(hi_f32(e2));
+          rs2 = add_f32x2(rs2, pack_f32x2(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(t_s + c * 16, pk);  // keys 32c..32c+31 -> bf16 pairs in columns 16c..16c+15
       }
+      const float rs = lo_f32(rs2) + hi_f32(rs2);
       l = l * alpha + rs;
-      // PV_{j-1} must be complete before P is overwritten and O is touched
-      if (j > 0 && !mbar_wait(b_odone, (j - 1) & 1, err, kErrAttnSoftmax)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      // O_x is quiescent until P_x(j) is released (PV_x(j-1) completed before S_x(j)):
+      // rescale it now if the max grew
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t u[32];
-          tmem_ld32(t_o + lane_off + c * 32, u);
+          tmem_ld32(t_o + c * 32, u);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(t_o + lane_off + c * 32, u);
-        }
-        tmem_wait_st();
-      }
-      // P row -> two swizzle atoms (keys 0..63, 64..127); 16-byte chunk c at c ^ (r & 7)
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int w0 = a * 32 + c * 4;
-          *reinterpret_cast<int4*>(prow + a * AT_ATOM + ((c ^ (r & 7)) << 4)) =
-              make_int4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
+          tmem_st32(t_o + c * 32, u);
         }
       }
-      fence_async_shared();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_pfull);
+      if (lane == 0) mbar_arrive(b_pfull + 8 * x);
     }
-    if (ok && mbar_wait(b_odone, (nt - 1) & 1, err, kErrAttnSoftmax)) {
+    if (ok && mbar_wait(b_odone, 0, err, kErrAttnSoftmax)) {
       tc_fence_after();
-      const int row = q0 + r;
+      const int row = q0 + x * AT_BM + r;
       const float inv = 1.f / l;
       bf16* dst = o + static_cast<size_t>(row) * nh * HD + h * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t u[32];
-        tmem_ld32(t_o + lane_off + c * 32, u);
+        tmem_ld32(t_o + c * 32, u);
         tmem_wait_ld();
         if (row < n_rows) {
 #pragma unroll
@@ -297,10 +364,15 @@ static cudaError_t launch_at(const bf16* q, const bf16* k, const bf16* vt, int l
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    // the register split above is only sound if the kernel launches with exactly this count
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, attention_tc_kernel<HD>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != AT_LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     configured = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  dim3 grid(cdiv(n_rows, AT_BM), nh);
+  dim3 grid(cdiv(n_rows, 2 * AT_BM), nh);
   attention_tc_kernel<HD><<<grid, AT_THREADS, C::SMEM, st>>>(tq, tk, tv, o, n_rows, nh, scale_log2, err);
   return cudaGetLastError();
 }

@@ -7,7 +7,7 @@
 //   warp 0      TMA producer: A tile 128x64 and B tile 256x64 per stage (128-byte swizzle)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128, N=256, K=16 steps)
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bias / SwiGLU / gate+residual, store
-//   warps 6..9  (INT8 only) dequantise the u8 codes of each stage into the swizzled bf16 B tile
+//   warps 6..13 (INT8 only) dequantise the u8 codes of each stage into the swizzled bf16 B tile
 // Two 256-column accumulators in TMEM let the epilogue of tile i overlap the mainloop of i+1.
 //
 // Epilogues ("minimax-h3-mlx" README, "Validation" and "AdaLN: measure, do not reason";
@@ -33,7 +33,7 @@ template <bool INT8>
 struct GemmCfg {
   static constexpr int STAGES = 4 - (INT8 ? 1 : 0);
   static constexpr int STAGE_BYTES = G_A_BYTES + G_B_BYTES + (INT8 ? G_Q_BYTES : 0);
-  static constexpr int THREADS = INT8 ? 320 : 192;
+  static constexpr int THREADS = INT8 ? 192 + 32 * 8 : 192;  // INT8: 8 dequant warps
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 };
 
@@ -182,24 +182,57 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
   }
 }
 
+// Per-thread modulation of one dequant stage: scale and qbias of the thread's four rows for
+// the group its 16-code chunk belongs to.  Loaded one stage ahead so the global latency hides
+// behind the current stage.
+struct DqScales {
+  float sc[4], qb[4];
+};
+
+__device__ __forceinline__ void dq_load_scales(const GemmParams& p, int brow0, int brow1, int kb, int t,
+                                               DqScales& d) {
+  const int g = kb * 2 + ((t & 3) >> 1);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = (t >> 2) + 64 * i;  // row within the 256-row tile
+    const int grow = (n < 128) ? brow0 + n : brow1 + (n - 128);
+    const bool ok = g < p.groups && grow < p.w_rows;
+    const size_t gi = static_cast<size_t>(grow) * p.groups + g;
+    d.sc[i] = ok ? bf2f(p.wscale[gi]) : 0.f;
+    d.qb[i] = ok ? bf2f(p.wqbias[gi]) : 0.f;
+  }
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Two codes (given as the f32 bit patterns 2^23 + code) -> bf16x2 of fma_f32(sc, code, qb):
+// the subtraction of 2^23 is exact, the fused multiply-add rounds once to f32 per lane, then
+// each lane is rounded to bf16 (nearest even).
+__device__ __forceinline__ uint32_t dq_pair(uint32_t m0, uint32_t m1, uint64_t sc2, uint64_t qb2) {
+  uint64_t v, r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(m0), "r"(m1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(v), "l"(0xCB000000CB000000ull));  // - 2^23
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(v) : "l"(r), "l"(sc2), "l"(qb2));
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+  return pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
+}
+
 // Dequantise one stage: u8 codes [256][64] (row-major, no swizzle) -> bf16 [256][64] in the
 // 128-byte swizzled K-major layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).
-// Thread t of the 128 dequant threads handles k-chunk (t & 3) (16 codes, one group) of rows
-// t/4 + 32 i; a warp therefore reads 512 contiguous code bytes per step.
-__device__ __forceinline__ void dequant_stage(const uint8_t* sq, uint8_t* sb, const GemmParams& p, int brow0, int brow1,
-                                              int kb, int t) {
+// Thread t of the 256 dequant threads handles k-chunk (t & 3) (16 codes, one group) of rows
+// t/4 + 64 i; a warp therefore reads 512 contiguous code bytes per step.
+__device__ __forceinline__ void dequant_stage(const uint8_t* sq, uint8_t* sb, const DqScales& d, int t) {
   const int kc = t & 3;
-  const int g = kb * 2 + (kc >> 1);
-#pragma unroll 2
-  for (int i = 0; i < 8; ++i) {
-    const int n = (t >> 2) + 32 * i;                  // row within the 256-row tile
-    const int grow = (n < 128) ? brow0 + n : brow1 + (n - 128);
-    float sc = 0.f, qb = 0.f;
-    if (g < p.groups && grow < p.w_rows) {
-      const size_t gi = static_cast<size_t>(grow) * p.groups + g;
-      sc = bf2f(p.wscale[gi]);
-      qb = bf2f(p.wqbias[gi]);
-    }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = (t >> 2) + 64 * i;
+    const uint64_t sc2 = (static_cast<uint64_t>(__float_as_uint(d.sc[i])) << 32) | __float_as_uint(d.sc[i]);
+    const uint64_t qb2 = (static_cast<uint64_t>(__float_as_uint(d.qb[i])) << 32) | __float_as_uint(d.qb[i]);
     const int4 codes = *reinterpret_cast<const int4*>(sq + n * 64 + kc * 16);
     const uint32_t cw[4] = {(uint32_t)codes.x, (uint32_t)codes.y, (uint32_t)codes.z, (uint32_t)codes.w};
     uint32_t o[8];
@@ -207,11 +240,10 @@ __device__ __forceinline__ void dequant_stage(const uint8_t* sq, uint8_t* sb, co
     for (int w = 0; w < 4; ++w) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t b0 = (cw[w] >> (16 * h)) & 0xFFu, b1 = (cw[w] >> (16 * h + 8)) & 0xFFu;
-        // exact u8 -> f32 through the 2^23 magic constant
-        const float f0 = __uint_as_float(0x4B000000u | b0) - 8388608.f;
-        const float f1 = __uint_as_float(0x4B000000u | b1) - 8388608.f;
-        o[2 * w + h] = pack_bf16x2(__fmaf_rn(sc, f0, qb), __fmaf_rn(sc, f1, qb));
+        // bytes 2h, 2h+1 of the word under the exponent byte of 2^23: exact u8 -> f32 pattern
+        const uint32_t m0 = prmt(cw[w], 0x4B000000u, 0x7540u + 2 * h);
+        const uint32_t m1 = prmt(cw[w], 0x4B000000u, 0x7541u + 2 * h);
+        o[2 * w + h] = dq_pair(m0, m1, sc2, qb2);
       }
     }
     uint8_t* rowp = sb + n * 128;
@@ -242,7 +274,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_ready + 8 * s, 4);
+      mbar_init(bar_ready + 8 * s, 8);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
@@ -348,28 +380,41 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       if (acc == 0) aph ^= 1;
     }
   } else if (INT8) {
-    const int t = threadIdx.x - 192;  // 0..127
+    const int t = threadIdx.x - 192;  // 0..255
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      int mb, nb;
-      tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
-      const int brow0 = nb * p.b_row_step, brow1 = brow0 + p.b_row1_off;
-      for (int kb = 0; kb < p.kb_count; ++kb) {
-        if (!mbar_wait(bar_full + 8 * s, ph, p.err, kErrGemmDequant)) {
-          ok = false;
-          break;
-        }
-        dequant_stage(sQ(s), sB(s), p, brow0, brow1, kb, t);
-        fence_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_ready + 8 * s);
-        if (++s == S) {
-          s = 0;
-          ph ^= 1;
-        }
+    // (tile, kb) sequence of this CTA, with the scales of the next stage loaded one step ahead
+    int tile = blockIdx.x, kb = 0, mb = 0, nb = 0;
+    if (tile < p.num_tiles) tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
+    DqScales cur, nxt;
+    if (tile < p.num_tiles) dq_load_scales(p, nb * p.b_row_step, nb * p.b_row_step + p.b_row1_off, 0, t, cur);
+    while (ok && tile < p.num_tiles) {
+      int tile2 = tile, kb2 = kb + 1, mb2 = mb, nb2 = nb;
+      if (kb2 == p.kb_count) {
+        kb2 = 0;
+        tile2 += gridDim.x;
+        if (tile2 < p.num_tiles) tile_coords(tile2, p.m_tiles, p.n_tiles, mb2, nb2);
       }
+      if (tile2 < p.num_tiles)
+        dq_load_scales(p, nb2 * p.b_row_step, nb2 * p.b_row_step + p.b_row1_off, kb2, t, nxt);
+      if (!mbar_wait(bar_full + 8 * s, ph, p.err, kErrGemmDequant)) {
+        ok = false;
+        break;
+      }
+      dequant_stage(sQ(s), sB(s), cur, t);
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ready + 8 * s);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
+      tile = tile2;
+      kb = kb2;
+      mb = mb2;
+      nb = nb2;
+      cur = nxt;
     }
   }
 
