@@ -155,6 +155,18 @@ h3_status h3_qknorm_rope(const h3_dims* dims, const void* qkv, const float* pos,
                          const void* k_norm, void* q_out, void* k_out, void* vt_out, int ld_vt, int n_rows,
                          void* workspace, size_t ws_bytes, void* stream);
 
+/* a2 + a3 -- the QKV projection with QK-norm and rotary embedding as one step, as the block
+ * runs it: q_out, k_out = RoPE(RMSNorm(.)) of xn Wqkv^T + b in the layout of h3_qknorm_rope,
+ * vt_out = v transposed.  With head_dim 128 (and without H3_F_UNFUSED) the norm and rotation
+ * run in the GEMM's epilogue and the projection never reaches memory; otherwise the projection
+ * goes to the workspace and h3_qknorm_rope's kernel follows.  xn: device bf16 [n_rows, H];
+ * wqkv: [3 nh hd, H] rows interleaved per head; workspace: device, 256-byte aligned, at least
+ * h3_qkv_project_workspace_size bytes (the per-row cos/sin table + room for the projection). */
+size_t h3_qkv_project_workspace_size(const h3_dims* dims, int n_rows);
+h3_status h3_qkv_project(const h3_dims* dims, const h3_linear* wqkv, const void* xn, const float* pos,
+                         const void* q_norm, const void* k_norm, void* q_out, void* k_out, void* vt_out, int ld_vt,
+                         int n_rows, void* workspace, size_t ws_bytes, unsigned flags, void* stream);
+
 /* a4 -- full unmasked self-attention ("minimax-h3-mlx" README, "Architecture"): per head,
  * o[r, h*hd + d] = sum_j softmax_j(q[h][r] . k[h][j] / sqrt(hd)) vt[h][d][j] over all j < n_rows.
  * q, k: device bf16 [nh][n_rows][hd]; vt: device bf16 [nh][hd][ld_vt]; o: device bf16
@@ -181,6 +193,16 @@ h3_status h3_attention(const h3_dims* dims, const void* q, const void* k, const 
 h3_status h3_qknorm_rope_static(const h3_dims* dims, const void* qkv, const float* pos, const void* q_norm,
                                 const void* k_norm, void* q_out, void* k_out, void* vt_out, int ld_vt, int n_rows,
                                 void* stream);
+
+/* Measurement hook.  h3_kernel_timer_start(capacity) creates `capacity` pairs of CUDA events
+ * (no device memory); from then on the first `capacity` attention launches made by
+ * h3_block_forward / h3_trunk_forward are each bracketed by an event pair recorded on the
+ * launching stream.  h3_kernel_timer_read waits for the recorded events, writes up to
+ * `capacity` per-launch durations in milliseconds to the host array `ms`, the number recorded
+ * to *n_recorded, and releases the events.  capacity 0 disarms.  Host-side state shared by
+ * every caller in the process (not thread-safe); meant for benchmarks. */
+h3_status h3_kernel_timer_start(int capacity);
+h3_status h3_kernel_timer_read(float* ms, int capacity, int* n_recorded);
 
 /* Synchronises `stream`, then reads and clears the device error word.  Returns H3_OK, or
  * H3_ETIMEOUT when a bounded device wait ran out since the last call (*site, if not NULL,

@@ -143,6 +143,25 @@ static bool check_indices(const uint8_t* tag, const int32_t* tidx, int n, int n_
   return true;
 }
 
+// a2 + a3: QKV projection, QK-norm and rotary embedding, q / k head-major and v transposed.
+// head_dim 128 on the tensor-core path: one GEMM whose epilogue does the norm and rotation
+// (the projection never goes to memory); otherwise the projection is written to `qkv_tmp`
+// ([n, 3 nh hd] bf16) and a second kernel does the norm and rotation.
+static cudaError_t qkv_step(const h3_dims& d, const h3_linear& wqkv, const bf16* xn, const float2* cs, const bf16* qn,
+                            const bf16* kn, bf16* q, bf16* k, bf16* vt, int ld_vt, int n, bf16* qkv_tmp,
+                            unsigned flags, cudaStream_t st) {
+  const int H = d.hidden, I = d.heads * d.head_dim;
+  if (!(flags & H3_F_UNFUSED) && d.head_dim == 128) {
+    LinearArgs a = make_linear(wqkv, kEpiQkv, xn, H, nullptr, 0, n);
+    a.qkv = QkvOut{d.heads, cs, qn, kn, d.qk_eps, q, k, vt, ld_vt};
+    return launch_linear_tc(a, st);
+  }
+  LinearArgs a = make_linear(wqkv, kEpiBias, xn, H, qkv_tmp, 3 * I, n);
+  cudaError_t e = run_linear(a, flags, st);
+  if (e != cudaSuccess) return e;
+  return launch_qknorm_rope(qkv_tmp, cs, qn, kn, d.qk_eps, q, k, vt, ld_vt, n, d.heads, d.head_dim, st);
+}
+
 // one block given a planned workspace whose rotary table is already filled
 static h3_status block_core(const h3_dims& d, const h3_block_w& w, const bf16* table_b, long long t_stride,
                             const bf16* x_in, bf16* x_out, int n, const uint8_t* tag, const int32_t* tidx,
@@ -152,20 +171,20 @@ static h3_status block_core(const h3_dims& d, const h3_block_w& w, const bf16* t
   cudaError_t e;
   // a1
   if ((e = launch_adaln_modulate(x_in, ws.xn, n, H, d.ln_eps, tr, 0, 1, st)) != cudaSuccess) return cuda_status(e);
-  // a2
-  LinearArgs a = make_linear(w.qkv, kEpiBias, ws.xn, H, ws.qkv, 3 * I, n);
-  if ((e = run_linear(a, flags, st)) != cudaSuccess) return cuda_status(e);
-  // a3
+  // a2 + a3
   const bool qk = !(flags & H3_F_NO_QKNORM) && w.q_norm && w.k_norm;
-  if ((e = launch_qknorm_rope(ws.qkv, ws.cs, qk ? static_cast<const bf16*>(w.q_norm) : nullptr,
-                              qk ? static_cast<const bf16*>(w.k_norm) : nullptr, d.qk_eps, ws.q, ws.k, ws.vt,
-                              ld_vt_for(n), n, d.heads, d.head_dim, st)) != cudaSuccess)
+  if ((e = qkv_step(d, w.qkv, ws.xn, ws.cs, qk ? static_cast<const bf16*>(w.q_norm) : nullptr,
+                    qk ? static_cast<const bf16*>(w.k_norm) : nullptr, ws.q, ws.k, ws.vt, ld_vt_for(n), n, ws.qkv,
+                    flags, st)) != cudaSuccess)
     return cuda_status(e);
+  LinearArgs a;
   // a4
+  timer_mark_begin(st);
   e = (flags & H3_F_UNFUSED)
           ? launch_attention_ref(ws.q, ws.k, ws.vt, ld_vt_for(n), ws.o, n, d.heads, d.head_dim, st)
           : launch_attention_tc(ws.q, ws.k, ws.vt, ld_vt_for(n), ws.o, n, d.heads, d.head_dim, error_word(), st);
   if (e != cudaSuccess) return cuda_status(e);
+  timer_mark_end(st);
   // a5: x_out = x_in + gate_msa * (o Wo^T + bo)
   a = make_linear(w.o, kEpiGateRes, ws.o, I, x_out, H, n);
   a.res = x_in;
@@ -302,6 +321,37 @@ h3_status h3_qknorm_rope(const h3_dims* dims, const void* qkv, const float* pos,
                            static_cast<const bf16*>(k_norm), dims->qk_eps, static_cast<bf16*>(q_out),
                            static_cast<bf16*>(k_out), static_cast<bf16*>(vt_out), ld_vt, n_rows, dims->heads,
                            dims->head_dim, st);
+  return cuda_status(e);
+}
+
+size_t h3_qkv_project_workspace_size(const h3_dims* dims, int n_rows) {
+  if (!dims_ok(dims) || n_rows < 0) return 0;
+  const size_t N = static_cast<size_t>(n_rows);
+  return align256(N * (dims->head_dim / 2) * sizeof(float2)) +
+         N * 3 * static_cast<size_t>(dims->heads) * dims->head_dim * 2;
+}
+
+h3_status h3_qkv_project(const h3_dims* dims, const h3_linear* wqkv, const void* xn, const float* pos,
+                         const void* q_norm, const void* k_norm, void* q_out, void* k_out, void* vt_out, int ld_vt,
+                         int n_rows, void* workspace, size_t ws_bytes, unsigned flags, void* stream) {
+  if (!dims_ok(dims) || !wqkv || !xn || !pos || !q_out || !k_out || !vt_out || n_rows < 0 || !workspace)
+    return H3_EINVAL;
+  const int H = dims->hidden, I = dims->heads * dims->head_dim;
+  if (!linear_ok(*wqkv, 3 * I, H) || ld_vt < n_rows || ld_vt % 8 || !aligned16(xn) || !aligned16(q_out) ||
+      !aligned16(k_out) || !aligned16(vt_out) || ((q_norm == nullptr) != (k_norm == nullptr)) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return H3_EINVAL;
+  if (ws_bytes < h3_qkv_project_workspace_size(dims, n_rows)) return H3_EINVAL;
+  if (n_rows == 0) return H3_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float2* cs = static_cast<float2*>(workspace);
+  bf16* tmp = reinterpret_cast<bf16*>(static_cast<char*>(workspace) +
+                                      align256(static_cast<size_t>(n_rows) * (dims->head_dim / 2) * sizeof(float2)));
+  cudaError_t e = launch_rope_table(pos, cs, n_rows, dims->head_dim, dims->rope_sections, dims->rope_theta, st);
+  if (e == cudaSuccess)
+    e = qkv_step(*dims, *wqkv, static_cast<const bf16*>(xn), cs, static_cast<const bf16*>(q_norm),
+                 static_cast<const bf16*>(k_norm), static_cast<bf16*>(q_out), static_cast<bf16*>(k_out),
+                 static_cast<bf16*>(vt_out), ld_vt, n_rows, tmp, flags, st);
   return cuda_status(e);
 }
 

@@ -52,8 +52,37 @@ struct GemmParams {
   const bf16* wqbias;
   int groups;          // K / 32
   int w_rows;          // rows of W (codes beyond it are TMA zero fill; their scales are not read)
+  // QKV epilogue (head_dim 128): column tile nb < nh holds head nb's q and k rows, tile
+  // nb >= nh the v rows of heads 2(nb - nh) and 2(nb - nh) + 1
+  int nh;
+  const float2* cs;    // [M][64] rotary (cos, sin)
+  const bf16* qn;      // [128] RMSNorm weights or null
+  const bf16* kn;
+  float qk_eps;
+  bf16* q;             // [nh][M][128]
+  bf16* k;
+  bf16* vt;            // [nh][128][ld_vt]
+  int ld_vt;
   unsigned* err;
 };
+
+// First row of each 128-row half of the B tile of column tile nb.
+template <int EPI>
+__device__ __forceinline__ void b_tile_rows(const GemmParams& p, int nb, int& r0, int& r1) {
+  if (EPI == kEpiQkv) {
+    if (nb < p.nh) {
+      r0 = nb * 384;          // q rows of head nb; its k rows follow
+      r1 = r0 + 128;
+    } else {
+      const int h0 = 2 * (nb - p.nh);
+      r0 = h0 * 384 + 256;    // v rows of heads h0 and h0 + 1
+      r1 = r0 + 384;
+    }
+  } else {
+    r0 = nb * p.b_row_step;
+    r1 = r0 + p.b_row1_off;
+  }
+}
 
 __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int& mb, int& nb) {
   const int per_group = GROUP_M * n_tiles;
@@ -90,11 +119,146 @@ __device__ __forceinline__ void store_row32(bf16* dst, const float* v, int valid
   }
 }
 
+__device__ __forceinline__ void load16_f32(const bf16* p, float* f) {
+  load8(p, f);
+  load8(p + 8, f + 8);
+}
+
+// QKV epilogue of one tile for the calling thread's row ("H3-metal" README, "Checkpoint layout
+// and media pipeline": QK normalisation and RoPE consume the per-head interleaved projection).
+// q|k tile (nb < nh): columns 0..127 are head nb's q, 128..255 its k.  Each thread owns one row,
+// so the RMS over 128 values and the rotary pairs (i, i + 64) stay in the thread: pass 1 reads
+// the accumulator for the two sums of squares, pass 2 re-reads it 8 pairs at a time, applies
+// bias, norm weight and rotation, and writes 256 contiguous bytes per head row.  v tile: two
+// heads' v rows, written transposed (warp lanes = consecutive rows, so each store instruction
+// covers 64 contiguous bytes).
+__device__ __forceinline__ void qkv_epilogue(const GemmParams& p, uint32_t tacc, int row, int nb) {
+  const bool row_ok = row < p.M;
+  if (nb < p.nh) {
+    const int h = nb;
+    const bf16* bh = p.bias ? p.bias + static_cast<size_t>(h) * 384 : nullptr;
+    float ssq = 0.f, ssk = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c * 32, r);
+      tmem_wait_ld();
+      float b[32];
+      if (bh) {
+        load16_f32(bh + c * 32, b);
+        load16_f32(bh + c * 32 + 16, b + 16);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) b[e] = 0.f;
+      }
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float v = __uint_as_float(r[e]) + b[e];
+        acc = fmaf(v, v, acc);
+      }
+      if (c < 4) ssq += acc;
+      else ssk += acc;
+    }
+    const bool has_norm = p.qn != nullptr && p.kn != nullptr;
+    const float rnq = has_norm ? rsqrtf(ssq / 128.f + p.qk_eps) : 1.f;
+    const float rnk = has_norm ? rsqrtf(ssk / 128.f + p.qk_eps) : 1.f;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {  // rotary pairs i = 8c .. 8c + 7
+      float cs_c[8], cs_s[8];
+      if (row_ok) {
+        const float4* src = reinterpret_cast<const float4*>(p.cs + static_cast<size_t>(row) * 64 + 8 * c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 v = __ldg(src + e);
+          cs_c[2 * e] = v.x;
+          cs_s[2 * e] = v.y;
+          cs_c[2 * e + 1] = v.z;
+          cs_s[2 * e + 1] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cs_c[e] = cs_s[e] = 0.f;
+      }
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        uint32_t ra[8], rb[8];
+        tmem_ld8(tacc + part * 128 + 8 * c, ra);
+        tmem_ld8(tacc + part * 128 + 64 + 8 * c, rb);
+        tmem_wait_ld();
+        float ba[8], bb[8], wa[8], wb[8];
+        if (bh) {
+          load8(bh + part * 128 + 8 * c, ba);
+          load8(bh + part * 128 + 64 + 8 * c, bb);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ba[e] = bb[e] = 0.f;
+        }
+        if (has_norm) {
+          const bf16* wn = part ? p.kn : p.qn;
+          load8(wn + 8 * c, wa);
+          load8(wn + 64 + 8 * c, wb);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) wa[e] = wb[e] = 1.f;
+        }
+        const float rn = part ? rnk : rnq;
+        uint32_t oa[4], ob[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float ya[2], yb[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int i = 2 * e + u;
+            const float xa = (__uint_as_float(ra[i]) + ba[i]) * rn * wa[i];
+            const float xb = (__uint_as_float(rb[i]) + bb[i]) * rn * wb[i];
+            ya[u] = xa * cs_c[i] - xb * cs_s[i];
+            yb[u] = xa * cs_s[i] + xb * cs_c[i];
+          }
+          oa[e] = pack_bf16x2(ya[0], ya[1]);
+          ob[e] = pack_bf16x2(yb[0], yb[1]);
+        }
+        if (row_ok) {
+          bf16* dst = (part ? p.k : p.q) + (static_cast<size_t>(h) * p.M + row) * 128;
+          *reinterpret_cast<int4*>(dst + 8 * c) = make_int4(oa[0], oa[1], oa[2], oa[3]);
+          *reinterpret_cast<int4*>(dst + 64 + 8 * c) = make_int4(ob[0], ob[1], ob[2], ob[3]);
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = 2 * (nb - p.nh) + hh;
+      const bf16* bh = (p.bias && h < p.nh) ? p.bias + static_cast<size_t>(h) * 384 + 256 : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tacc + hh * 128 + c * 32, r);
+        tmem_wait_ld();
+        if (!row_ok || h >= p.nh) continue;
+        float b[32];
+        if (bh) {
+          load16_f32(bh + c * 32, b);
+          load16_f32(bh + c * 32 + 16, b + 16);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) b[e] = 0.f;
+        }
+        bf16* dst = p.vt + (static_cast<size_t>(h) * 128 + c * 32) * p.ld_vt + row;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dst[static_cast<size_t>(e) * p.ld_vt] = f2bf(__uint_as_float(r[e]) + b[e]);
+      }
+    }
+  }
+}
+
 // Epilogue of one tile for the calling thread's row (TMEM lane = row within the tile).
 template <int EPI>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc, int row, int nb) {
   const bool row_ok = row < p.M;
-  if (EPI == kEpiSwiglu) {
+  if (EPI == kEpiQkv) {
+    qkv_epilogue(p, tacc, row, nb);
+  } else if (EPI == kEpiSwiglu) {
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t rg[32], rv[32];
@@ -307,7 +471,8 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         int mb, nb;
         tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
-        const int brow0 = nb * p.b_row_step, brow1 = brow0 + p.b_row1_off;
+        int brow0, brow1;
+        b_tile_rows<EPI>(p, nb, brow0, brow1);
         for (int kb = 0; kb < p.kb_count; ++kb) {
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, p.err, kErrGemmProducer)) {
             ok = false;
@@ -388,7 +553,11 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     int tile = blockIdx.x, kb = 0, mb = 0, nb = 0;
     if (tile < p.num_tiles) tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
     DqScales cur, nxt;
-    if (tile < p.num_tiles) dq_load_scales(p, nb * p.b_row_step, nb * p.b_row_step + p.b_row1_off, 0, t, cur);
+    int r0 = 0, r1 = 0;
+    if (tile < p.num_tiles) {
+      b_tile_rows<EPI>(p, nb, r0, r1);
+      dq_load_scales(p, r0, r1, 0, t, cur);
+    }
     while (ok && tile < p.num_tiles) {
       int tile2 = tile, kb2 = kb + 1, mb2 = mb, nb2 = nb;
       if (kb2 == p.kb_count) {
@@ -396,8 +565,10 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
         tile2 += gridDim.x;
         if (tile2 < p.num_tiles) tile_coords(tile2, p.m_tiles, p.n_tiles, mb2, nb2);
       }
-      if (tile2 < p.num_tiles)
-        dq_load_scales(p, nb2 * p.b_row_step, nb2 * p.b_row_step + p.b_row1_off, kb2, t, nxt);
+      if (tile2 < p.num_tiles) {
+        b_tile_rows<EPI>(p, nb2, r0, r1);
+        dq_load_scales(p, r0, r1, kb2, t, nxt);
+      }
       if (!mbar_wait(bar_full + 8 * s, ph, p.err, kErrGemmDequant)) {
         ok = false;
         break;
@@ -500,7 +671,22 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
   p.wqbias = a.wqbias;
   p.groups = a.K / 32;
   p.err = a.err;
-  const int w_rows = sw ? 2 * a.n_y : a.n_y;
+  int w_rows = sw ? 2 * a.n_y : a.n_y;
+  if (a.epi == kEpiQkv) {
+    // n_y = 3 * nh * 128 weight rows, tiled as nh q|k tiles and ceil(nh / 2) v tiles
+    p.nh = a.qkv.nh;
+    p.n_tiles = a.qkv.nh + (a.qkv.nh + 1) / 2;
+    p.num_tiles = p.m_tiles * p.n_tiles;
+    p.cs = a.qkv.cs;
+    p.qn = a.qkv.qn;
+    p.kn = a.qkv.kn;
+    p.qk_eps = a.qkv.eps;
+    p.q = a.qkv.q;
+    p.k = a.qkv.k;
+    p.vt = a.qkv.vt;
+    p.ld_vt = a.qkv.ld_vt;
+    w_rows = a.n_y;
+  }
   p.w_rows = w_rows;
 
   CUtensorMap ta, tb;
@@ -523,6 +709,8 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
     case kEpiSwiglu * 2 + 1: return launch_tc<kEpiSwiglu, true>(ta, tb, p, st);
     case kEpiGateRes * 2: return launch_tc<kEpiGateRes, false>(ta, tb, p, st);
     case kEpiGateRes * 2 + 1: return launch_tc<kEpiGateRes, true>(ta, tb, p, st);
+    case kEpiQkv * 2: return launch_tc<kEpiQkv, false>(ta, tb, p, st);
+    case kEpiQkv * 2 + 1: return launch_tc<kEpiQkv, true>(ta, tb, p, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -13,7 +13,21 @@ struct TableRef {
   const int32_t* tidx;
 };
 
-enum Epilogue : int { kEpiBias = 0, kEpiSwiglu = 1, kEpiGateRes = 2 };
+enum Epilogue : int { kEpiBias = 0, kEpiSwiglu = 1, kEpiGateRes = 2, kEpiQkv = 3 };
+
+// Fused QKV epilogue (head_dim 128): per-head RMSNorm of q and k (optional), rotary embedding
+// from the per-row cos/sin table, q and k written head-major, v written transposed.
+struct QkvOut {
+  int nh;
+  const float2* cs;  // [M][64]
+  const bf16* qn;    // [128] or null
+  const bf16* kn;
+  float eps;
+  bf16* q;           // [nh][M][128]
+  bf16* k;
+  bf16* vt;          // [nh][128][ld_vt]
+  int ld_vt;
+};
 
 // y = epilogue(x W^T + b).  W is bf16 [n_w_rows, K] or INT8-g32 codes + per-group scale/qbias.
 struct LinearArgs {
@@ -33,6 +47,7 @@ struct LinearArgs {
   const bf16* res;       // gate-residual input (stride ldy)
   TableRef gate;         // gate-residual gate
   int m_gate;
+  QkvOut qkv;            // kEpiQkv outputs
   unsigned* err;
 };
 
@@ -57,6 +72,10 @@ cudaError_t launch_attention_tc(const bf16* q, const bf16* k, const bf16* vt, in
                                 int hd, unsigned* err, cudaStream_t st);
 
 int num_sms();
+
+// measurement hooks (timer.cu): record the armed start / stop events around one launch
+void timer_mark_begin(cudaStream_t st);
+void timer_mark_end(cudaStream_t st);
 
 // cuTensorMapEncodeTiled fetched through the runtime's driver entry point (the library does not
 // link libcuda directly, so it loads on machines without a driver).

@@ -23,7 +23,8 @@ H3_EPI_BIAS, H3_EPI_SWIGLU, H3_EPI_GATE_RES = 0, 1, 2
 EXPORTS = (
     "h3_workspace_size", "h3_modcache_build", "h3_block_forward", "h3_trunk_forward", "h3_adaln_modulate",
     "h3_linear_forward", "h3_qknorm_rope", "h3_qknorm_rope_static", "h3_attention", "h3_last_device_error",
-    "h3_status_str",
+    "h3_status_str", "h3_kernel_timer_start", "h3_kernel_timer_read", "h3_qkv_project",
+    "h3_qkv_project_workspace_size",
 )
 
 # largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
@@ -72,8 +73,12 @@ def lib():
             "h3_linear_forward": (i32, [LW, i32, vp, i32, vp, i32, i32, vp, vp, i64, i32, vp, vp, u32, vp]),
             "h3_qknorm_rope": (i32, [D, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, vp]),
             "h3_qknorm_rope_static": (i32, [D, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp]),
+            "h3_qkv_project_workspace_size": (sz, [D, i32]),
+            "h3_qkv_project": (i32, [D, LW, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, u32, vp]),
             "h3_attention": (i32, [D, vp, vp, vp, i32, vp, i32, u32, vp]),
             "h3_last_device_error": (i32, [vp, ctypes.POINTER(u32)]),
+            "h3_kernel_timer_start": (i32, [i32]),
+            "h3_kernel_timer_read": (i32, [ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]),
             "h3_status_str": (ctypes.c_char_p, [i32]),
         }
         for name, (res, args) in sig.items():
@@ -143,8 +148,30 @@ def h3_qknorm_rope_static(dims, qkv, pos, q_norm, k_norm, q_out, k_out, vt_out, 
                                        n_rows, stream), "h3_qknorm_rope_static")
 
 
+def h3_qkv_project_workspace_size(dims, n_rows: int) -> int:
+    return lib().h3_qkv_project_workspace_size(ctypes.byref(dims), n_rows)
+
+
+def h3_qkv_project(dims, wqkv, xn, pos, q_norm, k_norm, q_out, k_out, vt_out, ld_vt, n_rows, workspace, ws_bytes,
+                   flags, stream):
+    _check(lib().h3_qkv_project(ctypes.byref(dims), ctypes.byref(wqkv), xn, pos, q_norm, k_norm, q_out, k_out, vt_out,
+                                ld_vt, n_rows, workspace, ws_bytes, flags, stream), "h3_qkv_project")
+
+
 def h3_attention(dims, q, k, vt, ld_vt, o, n_rows, flags, stream):
     _check(lib().h3_attention(ctypes.byref(dims), q, k, vt, ld_vt, o, n_rows, flags, stream), "h3_attention")
+
+
+def h3_kernel_timer_start(capacity: int):
+    _check(lib().h3_kernel_timer_start(capacity), "h3_kernel_timer_start")
+
+
+def h3_kernel_timer_read(capacity: int) -> list:
+    """Per-launch attention durations (ms) recorded since h3_kernel_timer_start."""
+    buf = (ctypes.c_float * max(capacity, 1))()
+    n = ctypes.c_int(0)
+    _check(lib().h3_kernel_timer_read(buf, capacity, ctypes.byref(n)), "h3_kernel_timer_read")
+    return [buf[i] for i in range(min(n.value, capacity))]
 
 
 def h3_last_device_error(stream):

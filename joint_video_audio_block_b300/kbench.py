@@ -29,7 +29,7 @@ import synth  # noqa: E402
 from joint_video_audio_block_b300 import h3  # noqa: E402
 from joint_video_audio_block_b300 import runtime as R  # noqa: E402
 
-KERNELS = ("attention", "qkv", "o", "fc1", "fc2", "adaln", "qkrope", "modcache")
+KERNELS = ("attention", "qkv", "o", "fc1", "fc2", "adaln", "qkrope", "qkvrope", "modcache")
 
 
 def _normal(shape, std=1.0, mean=0.0, stream=1):
@@ -119,6 +119,37 @@ def setup(kernel: str, n: int, int8: bool):
                               k.data_ptr(), vt.data_ptr(), ld, n, ws.data_ptr(), ws.numel(), st)
 
         return launch, 0.0, 12.0 * n * I + 12.0 * n + n * hd * 4.0 * 2, "includes the per-row cos/sin table", keep
+
+    if kernel == "qkvrope":
+        # a2 + a3 as the block runs them: the QKV GEMM with QK-norm + RoPE in its epilogue
+        xn = _normal((n, H), stream=18)
+        w = _normal((3 * I, H), 0.02, stream=19)
+        b = _normal((3 * I,), 0.02, stream=20)
+        wbytes = 2.0
+        if int8:
+            qc = torch.randint(0, 256, (3 * I, H), dtype=torch.uint8, device="cuda")
+            sc = _normal((3 * I, H // 32), 1e-3, stream=21)
+            qb = _normal((3 * I, H // 32), 0.02, stream=22)
+            lin = h3.make_linear(qc, b, sc, qb)
+            keep.append((qc, sc, qb))
+            wbytes = 1.0 + 4.0 / 32
+        else:
+            lin = h3.make_linear(w, b)
+        _, _, pos = synth.packed_rows(synth.CONFIGS["block12936"])
+        pos_d = torch.from_numpy(np.ascontiguousarray(np.resize(pos, (n, 3)))).cuda()
+        ld = (n + 63) // 64 * 64
+        q = torch.empty(nh, n, hd, dtype=torch.bfloat16, device="cuda")
+        k, vt = torch.empty_like(q), torch.empty(nh, hd, ld, dtype=torch.bfloat16, device="cuda")
+        qn, kn = _normal((hd,), 0.02, 1.0, stream=23), _normal((hd,), 0.02, 1.0, stream=24)
+        ws = torch.empty(h3.h3_qkv_project_workspace_size(dims, n), dtype=torch.uint8, device="cuda")
+        keep += [xn, w, b, lin, pos_d, q, k, vt, qn, kn, ws]
+
+        def launch():
+            h3.h3_qkv_project(dims, lin, xn.data_ptr(), pos_d.data_ptr(), qn.data_ptr(), kn.data_ptr(), q.data_ptr(),
+                              k.data_ptr(), vt.data_ptr(), ld, n, ws.data_ptr(), ws.numel(), 0, st)
+
+        byts = n * H * 2.0 + 3 * I * H * wbytes + 3.0 * n * I * 2 + n * hd * 4.0
+        return launch, 2.0 * n * H * 3 * I, byts, "includes the per-row cos/sin table kernel", keep
 
     if kernel == "modcache":
         T = n

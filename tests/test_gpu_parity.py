@@ -42,7 +42,7 @@ def check(gpu, ref, rel=REL_L2, abs_=MAX_ABS, what=""):
     assert r <= rel and mr <= abs_, f"{what}: rel_l2={r:.3e} (<= {rel}) max_abs/max|ref|={mr:.3e} (<= {abs_})"
 
 
-def check_step(gpu, ref, what="", spread=2e-3):
+def check_step(gpu, ref, what="", spread=2e-3, ulps=1, extra=None):
     """One step with identical bf16 inputs on both sides: the GPU output is the fp32 result
     rounded once to bf16, so each element is within 2^-8 |ref| (one bf16 ulp, covering the
     half-ulp rounding) plus `spread` x rms(ref) for fp32 accumulation order (and, for attention,
@@ -50,7 +50,9 @@ def check_step(gpu, ref, what="", spread=2e-3):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     r, m = _err(gpu, ref)
-    bound = 2.0 ** -8 * np.abs(ref) + spread * np.sqrt(np.mean(ref * ref))
+    bound = ulps * 2.0 ** -8 * np.abs(ref) + spread * np.sqrt(np.mean(ref * ref))
+    if extra is not None:
+        bound = bound + extra
     worst = float(np.max(np.abs(gpu - ref) - bound))
     print(f"{what}: rel_l2={r:.3e} max_abs={m:.3e} worst_excess={worst:.3e}")
     assert r <= 4e-3 and worst <= 0.0, f"{what}: rel_l2={r:.3e} excess over bf16 bound {worst:.3e}"
@@ -306,6 +308,51 @@ def test_qknorm_rope(name, qk):
     got_v = R.f32_from_bf16(vt)[:, :, : c.n].transpose(2, 0, 1)
     np.testing.assert_array_equal(got_v, rv)  # v is moved, not computed
     assert np.all(R.f32_from_bf16(vt)[:, :, c.n:] == 0)
+
+
+@pytest.mark.parametrize("name,flags,qk", [("block1829", 0, True), ("block1829", 0, False),
+                                          ("block1829", h3.H3_F_UNFUSED, True), ("tiny", 0, True), ("tiny", 0, False)])
+def test_qkv_project(name, flags, qk):
+    """a2 + a3 as the block runs them: projection, QK-norm and RoPE (fused into the GEMM epilogue
+    for head_dim 128), against the oracle's linear -> split -> RMSNorm -> RoPE on the same bf16
+    inputs.  The fused path rounds each output once (one bf16 ulp).  The two-kernel path (tiny's
+    head_dim 64, or H3_F_UNFUSED) also stores the projection in bf16 before the norm: that
+    rounding (<= 2^-8 |y|) reaches a rotated output through both members of its rotary pair, so
+    its bound adds 2^-8 (|x_i| + |x_(i+hd/2)|) of the normalised, unrotated pair."""
+    c = Case(name, qk_norm=qk)
+    d = c.d
+    xn_bits = synth.normal_bf16(6, 912, (c.n, d.hidden))
+    wt = R.upload_block(c.w_bits[0])
+    lin = h3.make_linear(wt["wqkv"], wt["bqkv"])
+    ld_vt = (c.n + 63) // 64 * 64
+    q = torch.empty(d.heads, c.n, d.head_dim, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty_like(q)
+    vt = torch.zeros(d.heads, d.head_dim, ld_vt, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(h3.h3_qkv_project_workspace_size(c.dims, c.n), dtype=torch.uint8, device="cuda")
+    xn = R.bf16_from_bits(xn_bits)
+    h3.h3_qkv_project(c.dims, lin, xn.data_ptr(), c.pos_d.data_ptr(), h3.ptr(wt.get("qnorm")), h3.ptr(wt.get("knorm")),
+                      q.data_ptr(), k.data_ptr(), vt.data_ptr(), ld_vt, c.n, ws.data_ptr(), ws.numel(), flags,
+                      h3.stream_ptr())
+    sync_ok()
+    y = O.linear(O.widen_bf16(xn_bits), O.widen_bf16(c.w_bits[0]["wqkv"]), O.widen_bf16(c.w_bits[0]["bqkv"]))
+    rq, rk, rv = O.split_qkv(y, d.heads, d.head_dim)
+    if qk:
+        rq = O.rms_norm(rq, O.widen_bf16(c.w_bits[0]["qnorm"]), d.qk_eps)
+        rk = O.rms_norm(rk, O.widen_bf16(c.w_bits[0]["knorm"]), d.qk_eps)
+    def pair_mag(x):
+        half = d.head_dim // 2
+        m = np.abs(x[..., :half]) + np.abs(x[..., half:])
+        return np.concatenate([m, m], axis=-1)
+
+    fused = d.head_dim == 128 and not flags
+    eq = None if fused else 2.0 ** -8 * pair_mag(rq)
+    ek = None if fused else 2.0 ** -8 * pair_mag(rk)
+    rq = O.rope(rq, c.pos, d.head_dim, d.rope_theta, d.rope_sections)
+    rk = O.rope(rk, c.pos, d.head_dim, d.rope_theta, d.rope_sections)
+    check_step(R.f32_from_bf16(q).transpose(1, 0, 2), rq, what=f"qkv_project q {name} f{flags}", extra=eq)
+    check_step(R.f32_from_bf16(k).transpose(1, 0, 2), rk, what=f"qkv_project k {name} f{flags}", extra=ek)
+    check_step(R.f32_from_bf16(vt)[:, :, : c.n].transpose(2, 0, 1), rv, what=f"qkv_project v {name} f{flags}")
+    assert np.all(R.f32_from_bf16(vt)[:, :, c.n:] == 0)  # the padding columns are not written
 
 
 def _attn_inputs(n, nh, hd, seed):
