@@ -67,6 +67,23 @@ def _attention_traffic(n_rows):
         return None
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest value of x over all ranks (x itself without a process group): the job's
+    time is the slowest replica's."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, rows: int, steps: int, seconds: float) -> float:
+    """Tokens per second of the whole job: every replica processes `rows` tokens per step."""
+    return world * rows * steps / seconds
+
+
 def _flops(cfg, n_rows):
     """(linear, attention) MMA FLOP of one block."""
     d = cfg.dims
@@ -268,16 +285,12 @@ def run_ours(args, cfg, rank, world, local_rank):
     att_durations = h3.h3_kernel_timer_read(B * args.steps)
     if dist:
         dist.barrier()
-    elapsed = ta.elapsed_time(tb) / 1e3
-    if dist:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(ta.elapsed_time(tb) / 1e3, dist, dev)
     st, site = h3.h3_last_device_error(sp)
     if st != h3.H3_OK:
         raise RuntimeError(f"device error in timed region: site {site:#x}")
     ms_per_step = elapsed / args.steps * 1e3
-    value = world * N * args.steps / elapsed
+    value = whole_job_rate(world, N, args.steps, elapsed)
 
     # end to end: host (pinned) inputs in, result out, every step
     xh = x0.cpu().pin_memory()
@@ -303,12 +316,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     for _ in range(args.steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * N * args.steps / e2e_s
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    e2e_value = whole_job_rate(world, N, args.steps, e2e_s)
 
     hbm_peak, bf16_peak, bf16_sus, peak_kind = _peaks()
     lin_f, att_f = _flops(cfg, N)

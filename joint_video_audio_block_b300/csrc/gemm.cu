@@ -7,7 +7,8 @@
 //   warp 0      TMA producer: A tile 128x64 and B tile 256x64 per stage (128-byte swizzle)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128, N=256, K=16 steps)
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bias / SwiGLU / gate+residual, store
-//   warps 6..13 (INT8 only) dequantise the u8 codes of each stage into the swizzled bf16 B tile
+//   warps 6..13 (INT8 only) load the u8 codes of each stage from global memory (three stages
+//               ahead, into registers) and write them dequantised into the swizzled bf16 B tile
 // Two 256-column accumulators in TMEM let the epilogue of tile i overlap the mainloop of i+1.
 //
 // Epilogues ("minimax-h3-mlx" README, "Validation" and "AdaLN: measure, do not reason";
@@ -26,13 +27,12 @@ namespace h3 {
 constexpr int G_BM = 128, G_BN = 256, G_BK = 64;
 constexpr int G_A_BYTES = G_BM * G_BK * 2;   // 16 KB
 constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
-constexpr int G_Q_BYTES = G_BN * G_BK;       // 16 KB of u8 codes (INT8 path)
 constexpr int GROUP_M = 16;                  // tile raster: 16 row-blocks per column sweep
 
 template <bool INT8>
 struct GemmCfg {
-  static constexpr int STAGES = 4 - (INT8 ? 1 : 0);
-  static constexpr int STAGE_BYTES = G_A_BYTES + G_B_BYTES + (INT8 ? G_Q_BYTES : 0);
+  static constexpr int STAGES = 4;
+  static constexpr int STAGE_BYTES = G_A_BYTES + G_B_BYTES;
   static constexpr int THREADS = INT8 ? 192 + 32 * 8 : 192;  // INT8: 8 dequant warps
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 };
@@ -48,6 +48,7 @@ struct GemmParams {
   const bf16* res;
   TableRef gate;
   int m_gate;
+  const void* wcodes;  // INT8: u8 [rows, K]
   const bf16* wscale;  // INT8: [rows, K/32]
   const bf16* wqbias;
   int groups;          // K / 32
@@ -346,22 +347,26 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
   }
 }
 
-// Per-thread modulation of one dequant stage: scale and qbias of the thread's four rows for
-// the group its 16-code chunk belongs to.  Loaded one stage ahead so the global latency hides
-// behind the current stage.
-struct DqScales {
+// One dequant stage of the calling thread: its four rows' 16-code chunk (k-chunk t & 3 of the
+// stage's 64 k) and the scale and qbias of the group that chunk belongs to.  Loaded from global
+// memory three stages ahead of use, so the loads overlap the dequantisation of earlier stages.
+struct DqStage {
+  int4 codes[4];
   float sc[4], qb[4];
 };
 
-__device__ __forceinline__ void dq_load_scales(const GemmParams& p, int brow0, int brow1, int kb, int t,
-                                               DqScales& d) {
-  const int g = kb * 2 + ((t & 3) >> 1);
+__device__ __forceinline__ void dq_load_stage(const GemmParams& p, const uint8_t* w, int brow0, int brow1, int kb,
+                                              int t, DqStage& d) {
+  const int kc = t & 3;
+  const int g = kb * 2 + (kc >> 1);
+  const int k0 = kb * 64 + kc * 16;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int n = (t >> 2) + 64 * i;  // row within the 256-row tile
     const int grow = (n < 128) ? brow0 + n : brow1 + (n - 128);
-    const bool ok = g < p.groups && grow < p.w_rows;
+    const bool ok = grow < p.w_rows && k0 < p.K;  // K % 32 == 0: a 16-code chunk is all in or all out
     const size_t gi = static_cast<size_t>(grow) * p.groups + g;
+    d.codes[i] = ok ? ld_nc_v4(w + static_cast<size_t>(grow) * p.K + k0) : make_int4(0, 0, 0, 0);
     d.sc[i] = ok ? bf2f(p.wscale[gi]) : 0.f;
     d.qb[i] = ok ? bf2f(p.wqbias[gi]) : 0.f;
   }
@@ -386,19 +391,18 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t m0, uint32_t m1, uint64_t s
   return pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
 }
 
-// Dequantise one stage: u8 codes [256][64] (row-major, no swizzle) -> bf16 [256][64] in the
-// 128-byte swizzled K-major layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).
-// Thread t of the 256 dequant threads handles k-chunk (t & 3) (16 codes, one group) of rows
-// t/4 + 64 i; a warp therefore reads 512 contiguous code bytes per step.
-__device__ __forceinline__ void dequant_stage(const uint8_t* sq, uint8_t* sb, const DqScales& d, int t) {
+// Dequantise one stage: the thread's codes -> bf16 [256][64] in the 128-byte swizzled K-major
+// layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).  Thread t of the 256 dequant
+// threads handles k-chunk (t & 3) (16 codes, one group) of rows t/4 + 64 i.
+__device__ __forceinline__ void dequant_stage(uint8_t* sb, const DqStage& d, int t) {
   const int kc = t & 3;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int n = (t >> 2) + 64 * i;
     const uint64_t sc2 = (static_cast<uint64_t>(__float_as_uint(d.sc[i])) << 32) | __float_as_uint(d.sc[i]);
     const uint64_t qb2 = (static_cast<uint64_t>(__float_as_uint(d.qb[i])) << 32) | __float_as_uint(d.qb[i]);
-    const int4 codes = *reinterpret_cast<const int4*>(sq + n * 64 + kc * 16);
-    const uint32_t cw[4] = {(uint32_t)codes.x, (uint32_t)codes.y, (uint32_t)codes.z, (uint32_t)codes.w};
+    const uint32_t cw[4] = {(uint32_t)d.codes[i].x, (uint32_t)d.codes[i].y, (uint32_t)d.codes[i].z,
+                            (uint32_t)d.codes[i].w};
     uint32_t o[8];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -461,7 +465,6 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
 
   auto sA = [&](int s) { return smem + s * C::STAGE_BYTES; };
   auto sB = [&](int s) { return smem + s * C::STAGE_BYTES + G_A_BYTES; };
-  auto sQ = [&](int s) { return smem + s * C::STAGE_BYTES + G_A_BYTES + G_B_BYTES; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -479,12 +482,9 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
             break;
           }
           const uint32_t fb = bar_full + 8 * s;
-          mbar_arrive_expect_tx(fb, G_A_BYTES + (INT8 ? G_Q_BYTES : G_B_BYTES));
+          mbar_arrive_expect_tx(fb, G_A_BYTES + (INT8 ? 0 : G_B_BYTES));
           tma_load_2d(smem_u32(sA(s)), &tmA, fb, kb * G_BK, mb * G_BM);
-          if (INT8) {
-            tma_load_2d(smem_u32(sQ(s)), &tmB, fb, kb * G_BK, brow0);
-            tma_load_2d(smem_u32(sQ(s)) + 128 * 64, &tmB, fb, kb * G_BK, brow1);
-          } else {
+          if (!INT8) {
             tma_load_2d(smem_u32(sB(s)), &tmB, fb, kb * G_BK, brow0);
             tma_load_2d(smem_u32(sB(s)) + 128 * 128, &tmB, fb, kb * G_BK, brow1);
           }
@@ -506,7 +506,8 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + acc * G_BN;
         for (int kb = 0; kb < p.kb_count; ++kb) {
-          if (!mbar_wait((INT8 ? bar_ready : bar_full) + 8 * s, ph, p.err, kErrGemmMma)) {
+          if (!mbar_wait(bar_full + 8 * s, ph, p.err, kErrGemmMma) ||
+              (INT8 && !mbar_wait(bar_ready + 8 * s, ph, p.err, kErrGemmMma))) {
             ok = false;
             break;
           }
@@ -546,34 +547,53 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     }
   } else if (INT8) {
     const int t = threadIdx.x - 192;  // 0..255
+    // The CTA's (tile, kb) stage sequence.  A stage's codes, scales and qbias are loaded into
+    // one of three register slots three stages ahead of their use; the loop is unrolled over
+    // the slots so no slot is ever copied (a copy would wait for the loads in flight).
+    struct Cursor {
+      int tile, kb, nb;
+    };
+    auto advance = [&](Cursor& c) {
+      if (++c.kb == p.kb_count) {
+        c.kb = 0;
+        c.tile += gridDim.x;
+        int mb;
+        if (c.tile < p.num_tiles) tile_coords(c.tile, p.m_tiles, p.n_tiles, mb, c.nb);
+      }
+    };
+    const uint8_t* wcodes = static_cast<const uint8_t*>(p.wcodes);
+    auto prefetch = [&](const Cursor& c, DqStage& d) {
+      if (c.tile < p.num_tiles) {
+        int r0, r1;
+        b_tile_rows<EPI>(p, c.nb, r0, r1);
+        dq_load_stage(p, wcodes, r0, r1, c.kb, t, d);
+      }
+    };
+    Cursor cur{static_cast<int>(blockIdx.x), 0, 0};
+    if (cur.tile < p.num_tiles) {
+      int mb;
+      tile_coords(cur.tile, p.m_tiles, p.n_tiles, mb, cur.nb);
+    }
+    Cursor ahead = cur;  // the stage whose scales are loaded next
+    DqStage d0, d1, d2;
+    prefetch(ahead, d0);
+    advance(ahead);
+    prefetch(ahead, d1);
+    advance(ahead);
+    prefetch(ahead, d2);
+    advance(ahead);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    // (tile, kb) sequence of this CTA, with the scales of the next stage loaded one step ahead
-    int tile = blockIdx.x, kb = 0, mb = 0, nb = 0;
-    if (tile < p.num_tiles) tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
-    DqScales cur, nxt;
-    int r0 = 0, r1 = 0;
-    if (tile < p.num_tiles) {
-      b_tile_rows<EPI>(p, nb, r0, r1);
-      dq_load_scales(p, r0, r1, 0, t, cur);
-    }
-    while (ok && tile < p.num_tiles) {
-      int tile2 = tile, kb2 = kb + 1, mb2 = mb, nb2 = nb;
-      if (kb2 == p.kb_count) {
-        kb2 = 0;
-        tile2 += gridDim.x;
-        if (tile2 < p.num_tiles) tile_coords(tile2, p.m_tiles, p.n_tiles, mb2, nb2);
-      }
-      if (tile2 < p.num_tiles) {
-        b_tile_rows<EPI>(p, nb2, r0, r1);
-        dq_load_scales(p, r0, r1, kb2, t, nxt);
-      }
-      if (!mbar_wait(bar_full + 8 * s, ph, p.err, kErrGemmDequant)) {
+    // one stage: wait until the MMA has released B slot s, dequantise slot d into it, then
+    // refill d three stages ahead
+    auto stage = [&](DqStage& d) {
+      if (!ok || cur.tile >= p.num_tiles) return;
+      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, p.err, kErrGemmDequant)) {
         ok = false;
-        break;
+        return;
       }
-      dequant_stage(sQ(s), sB(s), cur, t);
+      dequant_stage(sB(s), d, t);
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ready + 8 * s);
@@ -581,11 +601,14 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
         s = 0;
         ph ^= 1;
       }
-      tile = tile2;
-      kb = kb2;
-      mb = mb2;
-      nb = nb2;
-      cur = nxt;
+      prefetch(ahead, d);
+      advance(ahead);
+      advance(cur);
+    };
+    while (ok && cur.tile < p.num_tiles) {
+      stage(d0);
+      stage(d1);
+      stage(d2);
     }
   }
 
@@ -667,6 +690,7 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
   p.res = a.res;
   p.gate = a.gate;
   p.m_gate = a.m_gate;
+  p.wcodes = a.w;
   p.wscale = a.wscale;
   p.wqbias = a.wqbias;
   p.groups = a.K / 32;
