@@ -29,10 +29,18 @@ constexpr int G_A_BYTES = G_BM * G_BK * 2;   // 16 KB
 constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
 constexpr int GROUP_M = 16;                  // tile raster: 16 row-blocks per column sweep
 
+// bf16 weights: 128 x 256 tiles, two TMEM accumulators so the epilogue of one tile overlaps the
+// mainloop of the next.  INT8 weights: 256 x 256 tiles (two 128-row MMAs per k-step share each
+// dequantised B tile, halving the dequantisation per FLOP); the two accumulators fill TMEM, so
+// the epilogue does not overlap the next tile's mainloop.
 template <bool INT8>
 struct GemmCfg {
-  static constexpr int STAGES = 4;
-  static constexpr int STAGE_BYTES = G_A_BYTES + G_B_BYTES;
+  static constexpr int BM = INT8 ? 256 : 128;
+  static constexpr int MSUB = BM / 128;        // 128-row MMAs per k-step
+  static constexpr int NBUF = INT8 ? 1 : 2;    // accumulator buffers
+  static constexpr int A_BYTES = BM * G_BK * 2;
+  static constexpr int STAGES = INT8 ? 3 : 4;
+  static constexpr int STAGE_BYTES = A_BYTES + G_B_BYTES;
   static constexpr int THREADS = INT8 ? 192 + 32 * 8 : 192;  // INT8: 8 dequant warps
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 };
@@ -464,7 +472,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   auto sA = [&](int s) { return smem + s * C::STAGE_BYTES; };
-  auto sB = [&](int s) { return smem + s * C::STAGE_BYTES + G_A_BYTES; };
+  auto sB = [&](int s) { return smem + s * C::STAGE_BYTES + C::A_BYTES; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -482,8 +490,10 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
             break;
           }
           const uint32_t fb = bar_full + 8 * s;
-          mbar_arrive_expect_tx(fb, G_A_BYTES + (INT8 ? 0 : G_B_BYTES));
-          tma_load_2d(smem_u32(sA(s)), &tmA, fb, kb * G_BK, mb * G_BM);
+          mbar_arrive_expect_tx(fb, C::A_BYTES + (INT8 ? 0 : G_B_BYTES));
+#pragma unroll
+          for (int a = 0; a < C::MSUB; ++a)
+            tma_load_2d(smem_u32(sA(s)) + a * G_A_BYTES, &tmA, fb, kb * G_BK, mb * C::BM + a * 128);
           if (!INT8) {
             tma_load_2d(smem_u32(sB(s)), &tmB, fb, kb * G_BK, brow0);
             tma_load_2d(smem_u32(sB(s)) + 128 * 128, &tmB, fb, kb * G_BK, brow1);
@@ -504,7 +514,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1, p.err, kErrGemmMma)) break;
         tc_fence_after();
-        const uint32_t d = tmem_base + acc * G_BN;
+        const uint32_t d = tmem_base + acc * C::MSUB * G_BN;  // accumulator a of the tile at d + a * 256
         for (int kb = 0; kb < p.kb_count; ++kb) {
           if (!mbar_wait(bar_full + 8 * s, ph, p.err, kErrGemmMma) ||
               (INT8 && !mbar_wait(bar_ready + 8 * s, ph, p.err, kErrGemmMma))) {
@@ -515,7 +525,10 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
           const uint32_t a0 = smem_u32(sA(s)), b0 = smem_u32(sB(s));
 #pragma unroll
           for (int k = 0; k < G_BK / 16; ++k)
-            umma_bf16_ss(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
+#pragma unroll
+            for (int a = 0; a < C::MSUB; ++a)
+              umma_bf16_ss(d + a * G_BN, sdesc_k_sw128(a0 + a * G_A_BYTES + 32 * k), sdesc_k_sw128(b0 + 32 * k),
+                           idesc, (kb | k) != 0);
           umma_commit(bar_empty + 8 * s);
           if (++s == S) {
             s = 0;
@@ -524,8 +537,10 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
         }
         if (!ok) break;
         umma_commit(bar_tfull + 8 * acc);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1;
+        if (++acc == C::NBUF) {
+          acc = 0;
+          aph ^= 1;
+        }
       }
     }
   } else if (warp < 6) {
@@ -537,13 +552,18 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
       if (!mbar_wait(bar_tfull + 8 * acc, aph, p.err, kErrGemmEpilogue)) break;
       tc_fence_after();
-      const int row = mb * G_BM + quad * 32 + lane;
-      gemm_epilogue<EPI>(p, tmem_base + acc * G_BN + ((quad * 32) << 16), row, nb);
+#pragma unroll 1
+      for (int a = 0; a < C::MSUB; ++a) {
+        const int row = mb * C::BM + a * 128 + quad * 32 + lane;
+        gemm_epilogue<EPI>(p, tmem_base + (acc * C::MSUB + a) * G_BN + ((quad * 32) << 16), row, nb);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
-      acc ^= 1;
-      if (acc == 0) aph ^= 1;
+      if (++acc == C::NBUF) {
+        acc = 0;
+        aph ^= 1;
+      }
     }
   } else if (INT8) {
     const int t = threadIdx.x - 192;  // 0..255
@@ -677,7 +697,7 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
   p.M = a.M;
   p.K = a.K;
   p.n_y = a.n_y;
-  p.m_tiles = cdiv(a.M, G_BM);
+  p.m_tiles = cdiv(a.M, a.int8 ? GemmCfg<true>::BM : GemmCfg<false>::BM);
   const bool sw = a.epi == kEpiSwiglu;
   p.b_row_step = sw ? 128 : 256;
   p.b_row1_off = sw ? a.n_y : 128;
