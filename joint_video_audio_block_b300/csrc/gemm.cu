@@ -27,7 +27,11 @@ namespace h3 {
 constexpr int G_BM = 128, G_BN = 256, G_BK = 64;
 constexpr int G_A_BYTES = G_BM * G_BK * 2;   // 16 KB
 constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
-constexpr int GROUP_M = 16;                  // tile raster: 16 row-blocks per column sweep
+// Tile raster: column sweeps over groups of group_m row-blocks.  The host sizes group_m so a
+// group's A rows (group_m x 128 x K x 2 bytes) take about 48 MB of the 126 MB L2 and stay
+// resident while the sweep streams B once per group: B is read from HBM m_tiles / group_m
+// times, A once.
+constexpr size_t kRasterABytes = size_t(48) << 20;
 
 // bf16 weights: 128 x 256 tiles, two TMEM accumulators so the epilogue of one tile overlaps the
 // mainloop of the next.  INT8 weights: 256 x 256 tiles (two 128-row MMAs per k-step share each
@@ -48,6 +52,7 @@ struct GemmCfg {
 struct GemmParams {
   int M, K, n_y;
   int m_tiles, n_tiles, num_tiles, kb_count;
+  int group_m;      // row-blocks per raster group
   int b_row_step;   // B rows per column tile: 256 (plain) or 128 (SwiGLU)
   int b_row1_off;   // row offset of the second 128-row half of a B tile: 128, or n_y for SwiGLU
   const bf16* bias;
@@ -93,11 +98,11 @@ __device__ __forceinline__ void b_tile_rows(const GemmParams& p, int nb, int& r0
   }
 }
 
-__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int& mb, int& nb) {
-  const int per_group = GROUP_M * n_tiles;
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int group_m, int& mb, int& nb) {
+  const int per_group = group_m * n_tiles;
   const int g = tile / per_group;
-  const int first_m = g * GROUP_M;
-  const int gm = min(m_tiles - first_m, GROUP_M);
+  const int first_m = g * group_m;
+  const int gm = min(m_tiles - first_m, group_m);
   const int local = tile % per_group;
   mb = first_m + local % gm;
   nb = local / gm;
@@ -148,25 +153,24 @@ __device__ __forceinline__ void qkv_epilogue(const GemmParams& p, uint32_t tacc,
     const bf16* bh = p.bias ? p.bias + static_cast<size_t>(h) * 384 : nullptr;
     float ssq = 0.f, ssk = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tacc + c * 32, r);
+    for (int c = 0; c < 16; ++c) {
+      uint32_t r[16];
+      tmem_ld16(tacc + c * 16, r);
       tmem_wait_ld();
-      float b[32];
+      float b[16];
       if (bh) {
-        load16_f32(bh + c * 32, b);
-        load16_f32(bh + c * 32 + 16, b + 16);
+        load16_f32(bh + c * 16, b);
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) b[e] = 0.f;
+        for (int e = 0; e < 16; ++e) b[e] = 0.f;
       }
       float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 16; ++e) {
         const float v = __uint_as_float(r[e]) + b[e];
         acc = fmaf(v, v, acc);
       }
-      if (c < 4) ssq += acc;
+      if (c < 8) ssq += acc;
       else ssk += acc;
     }
     const bool has_norm = p.qn != nullptr && p.kn != nullptr;
@@ -481,7 +485,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         int mb, nb;
-        tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
+        tile_coords(tile, p.m_tiles, p.n_tiles, p.group_m, mb, nb);
         int brow0, brow1;
         b_tile_rows<EPI>(p, nb, brow0, brow1);
         for (int kb = 0; kb < p.kb_count; ++kb) {
@@ -549,7 +553,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mb, nb;
-      tile_coords(tile, p.m_tiles, p.n_tiles, mb, nb);
+      tile_coords(tile, p.m_tiles, p.n_tiles, p.group_m, mb, nb);
       if (!mbar_wait(bar_tfull + 8 * acc, aph, p.err, kErrGemmEpilogue)) break;
       tc_fence_after();
 #pragma unroll 1
@@ -578,7 +582,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
         c.kb = 0;
         c.tile += gridDim.x;
         int mb;
-        if (c.tile < p.num_tiles) tile_coords(c.tile, p.m_tiles, p.n_tiles, mb, c.nb);
+        if (c.tile < p.num_tiles) tile_coords(c.tile, p.m_tiles, p.n_tiles, p.group_m, mb, c.nb);
       }
     };
     const uint8_t* wcodes = static_cast<const uint8_t*>(p.wcodes);
@@ -592,7 +596,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     Cursor cur{static_cast<int>(blockIdx.x), 0, 0};
     if (cur.tile < p.num_tiles) {
       int mb;
-      tile_coords(cur.tile, p.m_tiles, p.n_tiles, mb, cur.nb);
+      tile_coords(cur.tile, p.m_tiles, p.n_tiles, p.group_m, mb, cur.nb);
     }
     Cursor ahead = cur;  // the stage whose scales are loaded next
     DqStage d0, d1, d2;
@@ -704,6 +708,13 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
   p.n_tiles = cdiv(a.n_y, p.b_row_step);
   p.num_tiles = p.m_tiles * p.n_tiles;
   p.kb_count = cdiv(a.K, G_BK);
+  {
+    const int bm = a.int8 ? GemmCfg<true>::BM : GemmCfg<false>::BM;
+    const size_t a_rows_bytes = static_cast<size_t>(bm) * a.K * 2;
+    int gm = static_cast<int>(kRasterABytes / (a_rows_bytes > 0 ? a_rows_bytes : 1));
+    p.group_m = gm < 4 ? 4 : (gm > p.m_tiles ? p.m_tiles : gm);
+    if (p.group_m < 1) p.group_m = 1;
+  }
   p.bias = a.bias;
   p.y = a.y;
   p.ldy = a.ldy;

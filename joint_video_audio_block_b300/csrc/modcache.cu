@@ -20,8 +20,10 @@ constexpr int MC_ROWS = 128, MC_K = 32, MC_TT = 5, MC_TMAX = 16 * MC_TT;
 __global__ void __launch_bounds__(256) modcache_kernel(const float* __restrict__ temb, int T, int Dt,
                                                        const bf16* __restrict__ W, const bf16* __restrict__ bias,
                                                        int n_out, bf16* __restrict__ table_b, long long t_stride) {
-  __shared__ float sw[MC_K][MC_ROWS + 4];   // k-major: a thread's 8 rows are 8 consecutive floats
-  __shared__ float st[MC_K][MC_TMAX + 4];
+  // k-major: a thread's 8 rows are 8 consecutive floats; the odd row pitches (129, 81 words)
+  // keep the transposing stores of the staging loops free of bank conflicts
+  __shared__ float sw[MC_K][MC_ROWS + 1];
+  __shared__ float st[MC_K][MC_TMAX + 1];
   const int j0 = blockIdx.x * MC_ROWS;
   const int t_base = blockIdx.y * MC_TMAX;
   const int tr = threadIdx.x & 15;          // timesteps t_base + tr + 16 i, i < 5

@@ -474,6 +474,61 @@ def test_block12936_sampled(name):
         print(f"int8 block vs bf16 masters: rel_l2={r:.3e} max_abs={m:.3e}")
 
 
+def test_block33720_sampled():
+    """Block 0 of the bench workload (768p 5 s Ref2VA canvas: 33,720 rows, condition image rows,
+    video and audio rows at different timesteps of the 77-entry table), checked on 256 sampled
+    query rows; keys and values come from every row."""
+    c = Case("trunk33720")
+    wt = R.upload_block(c.w_bits[0])
+    out = torch.empty_like(c.x)
+    _run_block(c, wt, c.x, out)
+    assert len(np.unique(c.tidx)) == 2 and c.T == 77  # two schedules in play
+    rows = np.sort(np.random.default_rng(11).choice(c.n, 256, replace=False))
+    ref = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows)
+    got = R.f32_from_bf16(out)[rows]
+    check(got, ref, what="block 33720 sampled")
+    emu = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows,
+                          emulate_bf16=True)
+    r_e, m_e = _err(emu, ref)
+    r_g, m_g = _err(got, ref)
+    print(f"bf16-storage oracle vs exact: rel_l2={r_e:.3e} max_abs={m_e:.3e}")
+    assert r_g <= 2 * r_e and m_g <= 2 * m_e
+
+
+def test_modcache_77_timesteps_full_width():
+    """The 40-step run's table: 77 distinct timesteps x 2 blocks x 18 x 5376 entries, every entry
+    within one bf16 ulp (plus the fp32 accumulation bound) of the exact projection."""
+    c = Case("trunk33720", n_blocks=2)
+    temb_d = torch.from_numpy(c.temb).cuda()
+    aw_d = [(R.bf16_from_bits(w), R.bf16_from_bits(b)) for w, b in c.aw]
+    table = torch.empty(c.T, 2, 18 * c.d.hidden, dtype=torch.bfloat16, device="cuda")
+    h3.h3_modcache_build(c.dims, temb_d.data_ptr(), c.T, c.d.temb_dim, [w.data_ptr() for w, _ in aw_d],
+                         [b.data_ptr() for _, b in aw_d], 2, table.data_ptr(), h3.stream_ptr())
+    sync_ok()
+    got = R.f32_from_bf16(table).astype(np.float64)
+    absum = np.stack([np.abs(c.temb.astype(np.float64)) @ np.abs(O.widen_bf16(w)).T + np.abs(O.widen_bf16(b))[None]
+                      for w, b in c.aw], axis=1)
+    excess = np.abs(got - c.table64) - (2.0 ** -8 * np.abs(c.table64) + 2.0 ** -20 * absum)
+    assert np.all(excess <= 0), excess.max()
+    assert np.mean(got == c.table_bf) > 0.99
+
+
+def test_trunk33720_equals_block_sequence():
+    """At the bench workload's size the trunk call is exactly two successive block calls."""
+    c = Case("trunk33720", n_blocks=2)
+    wts = [R.upload_block(w) for w in c.w_bits]
+    ws = R.workspace(c.dims, c.n)
+    x_seq = c.x.clone()
+    for b in range(2):
+        _run_block(c, wts[b], x_seq, x_seq, b=b)
+    x_tr = c.x.clone()
+    h3.h3_trunk_forward(c.dims, [h3.make_block_w(w) for w in wts], 2, c.table.data_ptr(), c.T, x_tr.data_ptr(), c.n,
+                        c.tag_d.data_ptr(), c.tidx_d.data_ptr(), c.pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0,
+                        h3.stream_ptr())
+    sync_ok()
+    assert torch.equal(x_tr, x_seq)
+
+
 def test_trunk_equals_block_sequence():
     c = Case("block1829", n_blocks=3)
     wts = [R.upload_block(w) for w in c.w_bits]
