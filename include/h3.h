@@ -204,6 +204,14 @@ h3_status h3_qknorm_rope_static(const h3_dims* dims, const void* qkv, const floa
 h3_status h3_kernel_timer_start(int capacity);
 h3_status h3_kernel_timer_read(float* ms, int capacity, int* n_recorded);
 
+/* Diagnostic of the failure path: launches one kernel whose mbarrier wait can never complete
+ * (nothing arrives), bounded by timeout_us (1 .. 1,000,000 microseconds).  The wait runs out,
+ * records site 0x301 in the device error word and the kernel ends normally, exactly as a
+ * stalled pipeline in any of the library's kernels would; the next h3_last_device_error then
+ * reports H3_ETIMEOUT with that site and the context stays usable.  No fault or trap is
+ * involved.  timeout_us outside the range returns H3_EINVAL. */
+h3_status h3_diag_expire_wait(unsigned timeout_us, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device error word.  Returns H3_OK, or
  * H3_ETIMEOUT when a bounded device wait ran out since the last call (*site, if not NULL,
  * receives the site code), or H3_ECUDA if the stream reports a CUDA error. */

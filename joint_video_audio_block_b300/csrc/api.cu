@@ -24,7 +24,10 @@ namespace h3 {
 
 __device__ unsigned g_error_word;  // first error site recorded by a bounded device wait
 
-static unsigned* error_word() {
+unsigned* error_word();
+unsigned* h3_error_word_ptr() { return error_word(); }
+
+unsigned* error_word() {
   static unsigned* ptr[64] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;

@@ -22,6 +22,7 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s per wait
 enum ErrSite : unsigned {
   kErrGemmProducer = 0x101, kErrGemmMma = 0x102, kErrGemmEpilogue = 0x103, kErrGemmDequant = 0x104,
   kErrAttnProducer = 0x201, kErrAttnMma = 0x202, kErrAttnSoftmax = 0x203,
+  kErrDiagWait = 0x301,  // the diagnostic wait of h3_diag_expire_wait
 };
 
 __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -83,14 +84,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed.  Returns false (after recording
 // `site`) on timeout or when another CTA has already reported an error.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, unsigned site) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, unsigned site,
+                                          unsigned long long timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 1023u) == 0) {
       if (err && *reinterpret_cast<volatile unsigned*>(err) != 0u) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (globaltimer() - t0 > timeout_ns) {
         record_error(err, site);
         return false;
       }

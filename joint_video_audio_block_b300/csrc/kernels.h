@@ -73,6 +73,9 @@ cudaError_t launch_attention_tc(const bf16* q, const bf16* k, const bf16* vt, in
 
 int num_sms();
 
+// device address of the library's error word on the current device (api.cu)
+unsigned* h3_error_word_ptr();
+
 // measurement hooks (timer.cu): record the armed start / stop events around one launch
 void timer_mark_begin(cudaStream_t st);
 void timer_mark_end(cudaStream_t st);

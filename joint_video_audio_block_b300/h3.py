@@ -24,7 +24,7 @@ EXPORTS = (
     "h3_workspace_size", "h3_modcache_build", "h3_block_forward", "h3_trunk_forward", "h3_adaln_modulate",
     "h3_linear_forward", "h3_qknorm_rope", "h3_qknorm_rope_static", "h3_attention", "h3_last_device_error",
     "h3_status_str", "h3_kernel_timer_start", "h3_kernel_timer_read", "h3_qkv_project",
-    "h3_qkv_project_workspace_size",
+    "h3_qkv_project_workspace_size", "h3_diag_expire_wait",
 )
 
 # largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
@@ -78,6 +78,7 @@ def lib():
             "h3_attention": (i32, [D, vp, vp, vp, i32, vp, i32, u32, vp]),
             "h3_last_device_error": (i32, [vp, ctypes.POINTER(u32)]),
             "h3_kernel_timer_start": (i32, [i32]),
+            "h3_diag_expire_wait": (i32, [u32, vp]),
             "h3_kernel_timer_read": (i32, [ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]),
             "h3_status_str": (ctypes.c_char_p, [i32]),
         }
@@ -172,6 +173,10 @@ def h3_kernel_timer_read(capacity: int) -> list:
     n = ctypes.c_int(0)
     _check(lib().h3_kernel_timer_read(buf, capacity, ctypes.byref(n)), "h3_kernel_timer_read")
     return [buf[i] for i in range(min(n.value, capacity))]
+
+
+def h3_diag_expire_wait(timeout_us: int, stream):
+    _check(lib().h3_diag_expire_wait(timeout_us, stream), "h3_diag_expire_wait")
 
 
 def h3_last_device_error(stream):

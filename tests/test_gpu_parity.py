@@ -554,6 +554,34 @@ def test_trunk_equals_block_sequence():
 # ----------------------------------------------------------------------------- edges / errors
 
 
+def test_bounded_wait_expires_and_context_survives():
+    """Failure path without a fault: a pipeline wait that can never complete runs out after its
+    limit, the device error word reports it as H3_ETIMEOUT, and the context keeps working."""
+    st = h3.stream_ptr()
+    sync_ok()
+    with pytest.raises(h3.H3Error):
+        h3.h3_diag_expire_wait(0, st)  # refused on the host
+    h3.h3_diag_expire_wait(2000, st)  # 2 ms limit
+    status, site = h3.h3_last_device_error(st)
+    assert status == h3.H3_ETIMEOUT and site == 0x301
+    status, site = h3.h3_last_device_error(st)  # read-and-clear
+    assert status == h3.H3_OK and site == 0
+    # a real kernel afterwards still runs and still matches the oracle
+    n, nh, hd = 130, 2, 128
+    q, k, v = _attn_inputs(n, nh, hd, seed=5)
+    ld_vt = (n + 63) // 64 * 64
+    vt = np.zeros((nh, hd, ld_vt), np.uint16)
+    vt[:, :, :n] = v.transpose(0, 2, 1)
+    o = torch.empty(n, nh * hd, dtype=torch.bfloat16, device="cuda")
+    dims = h3.make_dims(nh * hd, nh, hd, 128, (hd // 8, 3 * hd // 16, 3 * hd // 16))
+    qd, kd, vd = R.bf16_from_bits(q), R.bf16_from_bits(k), R.bf16_from_bits(vt)
+    h3.h3_attention(dims, qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), ld_vt, o.data_ptr(), n, 0, st)
+    sync_ok()
+    t = lambda a: O.widen_bf16(a).transpose(1, 0, 2)  # noqa: E731
+    ref = O.attention(t(q), t(k), t(v)).reshape(n, nh * hd)
+    check_step(R.f32_from_bf16(o), ref, what="attention after an expired wait", spread=1e-2)
+
+
 def test_zero_rows_and_bad_arguments():
     c = Case("tiny")
     wt = R.upload_block(c.w_bits[0])
