@@ -174,6 +174,17 @@ h3_status h3_qkv_project(const h3_dims* dims, const h3_linear* wqkv, const void*
 h3_status h3_attention(const h3_dims* dims, const void* q, const void* k, const void* vt, int ld_vt, void* o,
                        int n_rows, unsigned flags, void* stream);
 
+/* Block-sparse variant of h3_attention (video sparse attention style: attention restricted to
+ * selected tiles; the pages' own sparse backend uses trained tile masks, which are not part of
+ * this library -- the caller supplies the mask).  The sequence is cut into 128-row tiles,
+ * nt = ceil(n_rows / 128) query tiles and as many key tiles; tile_mask: device u8
+ * [nh][nt][nt], tile_mask[h][qi][kj] != 0 keeps key tile kj for query tile qi of head h, and
+ * every score outside the kept tiles counts as -inf.  A query row that keeps no key tile gets an
+ * all-zero output row.  Work scales with the kept tiles (the kernel skips a key tile that both
+ * query tiles of its 256-row pair drop).  Other arguments and layouts as h3_attention. */
+h3_status h3_attention_sparse(const h3_dims* dims, const void* q, const void* k, const void* vt, int ld_vt, void* o,
+                              int n_rows, const uint8_t* tile_mask, void* stream);
+
 /* h3_qknorm_rope without a caller-supplied workspace.  The pages have no counterpart: this
  * entry point exists for callers that cannot allocate device memory at the call site (an
  * embedder whose device memory belongs to a pool or allocator it cannot reach there, or a

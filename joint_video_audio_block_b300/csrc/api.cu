@@ -372,6 +372,17 @@ h3_status h3_attention(const h3_dims* dims, const void* q, const void* k, const 
   return cuda_status(e);
 }
 
+h3_status h3_attention_sparse(const h3_dims* dims, const void* q, const void* k, const void* vt, int ld_vt, void* o,
+                              int n_rows, const uint8_t* tile_mask, void* stream) {
+  if (!dims_ok(dims) || !q || !k || !vt || !o || !tile_mask || n_rows < 0 || ld_vt < n_rows || ld_vt % 8)
+    return H3_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o)) return H3_EINVAL;
+  return cuda_status(launch_attention_sparse_tc(static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                                                static_cast<const bf16*>(vt), ld_vt, static_cast<bf16*>(o), n_rows,
+                                                dims->heads, dims->head_dim, tile_mask, error_word(),
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 h3_status h3_block_forward(const h3_dims* dims, const h3_block_w* w, const void* table_b, long long t_stride, int T,
                            const void* x_in, void* x_out, int n_rows, const uint8_t* tag, const int32_t* tidx,
                            const float* pos, void* workspace, size_t ws_bytes, unsigned flags, void* stream) {

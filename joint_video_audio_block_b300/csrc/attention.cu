@@ -98,11 +98,15 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
-template <int HD>
+// SPARSE: block-sparse attention over 128 x 128 (query tile, key tile) blocks.  mask[h][qi][kj]
+// != 0 keeps key tile kj for query tile qi of head h; every other score is -inf.  The CTA
+// loads the key tiles either of its two query tiles keeps, and each query tile multiplies and
+// normalises only the ones it keeps.  A query row that keeps no key tile gets a zero output.
+template <int HD, bool SPARSE>
 __global__ void __launch_bounds__(AT_THREADS, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, bf16* __restrict__ o, int n_rows, int nh,
-                        float scale_log2, unsigned* err) {
+                        float scale_log2, const uint8_t* __restrict__ mask, unsigned* err) {
   using C = AtCfg<HD>;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -121,6 +125,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const int h = blockIdx.y;
   const int q0 = blockIdx.x * 2 * AT_BM;
   const int nt = cdiv(n_rows, AT_BN);
+  // key-tile masks of this CTA's two query tiles (dense: every tile kept)
+  const int qt = cdiv(n_rows, AT_BM);
+  const uint8_t* mask_a = SPARSE ? mask + (static_cast<size_t>(h) * qt + 2 * blockIdx.x) * nt : nullptr;
+  const uint8_t* mask_b = (SPARSE && 2 * blockIdx.x + 1 < qt) ? mask_a + nt : nullptr;
+  auto keep = [&](int x, int j) -> bool {
+    if (!SPARSE) return true;
+    const uint8_t* m = x ? mask_b : mask_a;
+    return m != nullptr && m[j] != 0;
+  };
+  // the key tiles the CTA visits, in order: next_tile(j) = first kept tile >= j (nt if none)
+  auto next_tile = [&](int j) -> int {
+    if (SPARSE)
+      while (j < nt && !keep(0, j) && !keep(1, j)) ++j;
+    return j;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
@@ -162,9 +181,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       for (int x = 0; x < 2; ++x)
         for (int a = 0; a < HD / 64; ++a)
           tma_load_3d(sQ + x * C::QK_TILE + a * AT_ATOM, &tmQ, b_q, 64 * a, q0 + x * AT_BM, h);
-      for (int j = 0; j < nt; ++j) {
-        const int s = j % ST;
-        if (!mbar_wait(b_kvempty + 8 * s, ((j / ST) & 1) ^ 1, err, kErrAttnProducer)) break;
+      for (int it = 0, j = next_tile(0); j < nt; ++it, j = next_tile(j + 1)) {
+        const int s = it % ST;
+        if (!mbar_wait(b_kvempty + 8 * s, ((it / ST) & 1) ^ 1, err, kErrAttnProducer)) break;
         const uint32_t kd = sK + s * C::QK_TILE, vd = sV + s * C::V_TILE;
         mbar_arrive_expect_tx(b_kfull + 8 * s, C::QK_TILE);
         for (int a = 0; a < HD / 64; ++a) tma_load_3d(kd + a * AT_ATOM, &tmK, b_kfull + 8 * s, 64 * a, j * AT_BN, h);
@@ -177,8 +196,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD);
-      auto issue_s = [&](int x, int j) {  // S_x(j) = Q_x K_j^T
-        const uint32_t kb = sK + (j % ST) * C::QK_TILE, qb = sQ + x * C::QK_TILE;
+      // it = position of the key tile in the CTA's visiting order (selects ring stage and phase)
+      auto issue_s = [&](int x, int it) {  // S_x = Q_x K^T for visited tile it
+        const uint32_t kb = sK + (it % ST) * C::QK_TILE, qb = sQ + x * C::QK_TILE;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * AT_ATOM + (kk & 3) * 32;
@@ -186,38 +206,61 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         umma_commit(b_sfull + 8 * x);
       };
-      auto issue_pv = [&](int x, int j) {  // O_x += P_x(j) V_j
-        const uint32_t vb = sV + (j % ST) * C::V_TILE;
+      auto issue_pv = [&](int x, int it, int first) {  // O_x (+)= P_x V for visited tile it
+        const uint32_t vb = sV + (it % ST) * C::V_TILE;
 #pragma unroll
         for (int kk = 0; kk < AT_BN / 16; ++kk)
           umma_bf16_ts(tmem + 256 + x * HD, tmem + x * 128 + kk * 8,
-                       sdesc_k_sw128(vb + (kk >> 2) * C::V_ATOM + (kk & 3) * 32), idesc_o, (j | kk) != 0);
+                       sdesc_k_sw128(vb + (kk >> 2) * C::V_ATOM + (kk & 3) * 32), idesc_o, !(first && kk == 0));
       };
-      bool ok = mbar_wait(b_q, 0, err, kErrAttnMma) && mbar_wait(b_kfull, 0, err, kErrAttnMma);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-      }
-      for (int j = 0; ok && j < nt; ++j) {
-        const int s = j % ST;
-        const uint32_t par = (j / ST) & 1;
-        const bool more = j + 1 < nt;
-        // tile A: P_A(j) V_j, then S_A(j+1)
-        if (!mbar_wait(b_pfull, j & 1, err, kErrAttnMma) || !mbar_wait(b_vfull + 8 * s, par, err, kErrAttnMma)) break;
-        tc_fence_after();
-        issue_pv(0, j);
-        if (more) {
-          if (!mbar_wait(b_kfull + 8 * ((j + 1) % ST), ((j + 1) / ST) & 1, err, kErrAttnMma)) break;
+      // Each query tile runs its own sequence over the key tiles it keeps (all of them when
+      // dense); cnt[x] counts tile x's S / P phases.  S_x of the next kept tile is issued right
+      // after PV_x of the current one, so it may overwrite P_x in TMEM (in-order execution).
+      int j = next_tile(0);
+      int cnt[2] = {0, 0};
+      bool ok = mbar_wait(b_q, 0, err, kErrAttnMma);
+      if (ok && j < nt) {
+        ok = mbar_wait(b_kfull, 0, err, kErrAttnMma);
+        if (ok) {
           tc_fence_after();
-          issue_s(0, j + 1);
+          if (keep(0, j)) issue_s(0, 0);
+          if (keep(1, j)) issue_s(1, 0);
         }
-        // tile B: P_B(j) V_j, release K_j / V_j, then S_B(j+1)
-        if (!mbar_wait(b_pfull + 8, j & 1, err, kErrAttnMma)) break;
-        tc_fence_after();
-        issue_pv(1, j);
-        umma_commit(b_kvempty + 8 * s);
-        if (more) issue_s(1, j + 1);
+      }
+      for (int it = 0; ok && j < nt; ++it) {
+        const int s = it % ST;
+        const uint32_t par = (it / ST) & 1;
+        const int jn = next_tile(j + 1);
+        const bool more = jn < nt;
+        bool v_ready = false, k_ready = false;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (keep(x, j)) {  // P_x V for this tile
+            if (!mbar_wait(b_pfull + 8 * x, cnt[x] & 1, err, kErrAttnMma)) {
+              ok = false;
+              break;
+            }
+            if (!v_ready && !mbar_wait(b_vfull + 8 * s, par, err, kErrAttnMma)) {
+              ok = false;
+              break;
+            }
+            v_ready = true;
+            tc_fence_after();
+            issue_pv(x, it, cnt[x] == 0);
+            ++cnt[x];
+          }
+          if (x == 1) umma_commit(b_kvempty + 8 * s);  // K / V of this stage are no longer read
+          if (more && keep(x, jn)) {  // S_x of the next visited tile
+            if (!k_ready && !mbar_wait(b_kfull + 8 * ((it + 1) % ST), ((it + 1) / ST) & 1, err, kErrAttnMma)) {
+              ok = false;
+              break;
+            }
+            k_ready = true;
+            tc_fence_after();
+            issue_s(x, it + 1);
+          }
+        }
+        j = jn;
       }
       if (ok) umma_commit(b_odone);
     }
@@ -232,11 +275,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t t_o = tmem + lane_off + 256 + x * HD;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      if (!mbar_wait(b_sfull + 8 * x, j & 1, err, kErrAttnSoftmax)) {
+    int cnt = 0;  // S / P phases of this query tile = key tiles it keeps
+    for (int j = next_tile(0); j < nt; j = next_tile(j + 1)) {
+      if (SPARSE && !keep(x, j)) continue;  // visited for the other query tile only
+      if (!mbar_wait(b_sfull + 8 * x, cnt & 1, err, kErrAttnSoftmax)) {
         ok = false;
         break;
       }
+      ++cnt;
       tc_fence_after();
       uint32_t sv[128];
 #pragma unroll
@@ -263,7 +309,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * scale_log2;
       float alpha = 1.f;
       bool rescale = false;
-      if (j == 0) {
+      if (m_used == -INFINITY) {  // first tile this query tile keeps
         m_used = mt;
       } else if (mt > m_used + AT_RESCALE_THRESHOLD) {
         alpha = ex2f(m_used - mt);
@@ -309,7 +355,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (ok && mbar_wait(b_odone, 0, err, kErrAttnSoftmax)) {
       tc_fence_after();
       const int row = q0 + x * AT_BM + r;
-      const float inv = 1.f / l;
+      const float inv = l > 0.f ? 1.f / l : 0.f;  // a row that kept no key tile outputs zeros
       bf16* dst = o + static_cast<size_t>(row) * nh * HD + h * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
@@ -322,7 +368,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(u[8 * q + 2 * e]) * inv, __uint_as_float(u[8 * q + 2 * e + 1]) * inv);
+              w[e] = l > 0.f ? pack_bf16x2(__uint_as_float(u[8 * q + 2 * e]) * inv,
+                                           __uint_as_float(u[8 * q + 2 * e + 1]) * inv)
+                             : 0u;  // O was never written (or is all zero): do not read it
             reinterpret_cast<int4*>(dst + c * 32)[q] = make_int4(w[0], w[1], w[2], w[3]);
           }
         }
@@ -349,9 +397,9 @@ static bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HD>
+template <int HD, bool SPARSE>
 static cudaError_t launch_at(const bf16* q, const bf16* k, const bf16* vt, int ld_vt, bf16* o, int n_rows, int nh,
-                             unsigned* err, cudaStream_t st) {
+                             const uint8_t* mask, unsigned* err, cudaStream_t st) {
   using C = AtCfg<HD>;
   CUtensorMap tq, tk, tv;
   const uint64_t rs = static_cast<uint64_t>(HD) * 2;
@@ -362,26 +410,35 @@ static cudaError_t launch_at(const bf16* q, const bf16* k, const bf16* vt, int l
     return cudaErrorInvalidValue;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(attention_tc_kernel<HD, SPARSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     // the register split above is only sound if the kernel launches with exactly this count
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, attention_tc_kernel<HD>);
+    e = cudaFuncGetAttributes(&fa, attention_tc_kernel<HD, SPARSE>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != AT_LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     configured = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   dim3 grid(cdiv(n_rows, 2 * AT_BM), nh);
-  attention_tc_kernel<HD><<<grid, AT_THREADS, C::SMEM, st>>>(tq, tk, tv, o, n_rows, nh, scale_log2, err);
+  attention_tc_kernel<HD, SPARSE><<<grid, AT_THREADS, C::SMEM, st>>>(tq, tk, tv, o, n_rows, nh, scale_log2, mask, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attention_tc(const bf16* q, const bf16* k, const bf16* vt, int ld_vt, bf16* o, int n_rows, int nh,
                                 int hd, unsigned* err, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
-  if (hd == 128) return launch_at<128>(q, k, vt, ld_vt, o, n_rows, nh, err, st);
-  if (hd == 64) return launch_at<64>(q, k, vt, ld_vt, o, n_rows, nh, err, st);
+  if (hd == 128) return launch_at<128, false>(q, k, vt, ld_vt, o, n_rows, nh, nullptr, err, st);
+  if (hd == 64) return launch_at<64, false>(q, k, vt, ld_vt, o, n_rows, nh, nullptr, err, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention_sparse_tc(const bf16* q, const bf16* k, const bf16* vt, int ld_vt, bf16* o, int n_rows,
+                                       int nh, int hd, const uint8_t* mask, unsigned* err, cudaStream_t st) {
+  if (n_rows <= 0) return cudaSuccess;
+  if (hd == 128) return launch_at<128, true>(q, k, vt, ld_vt, o, n_rows, nh, mask, err, st);
+  if (hd == 64) return launch_at<64, true>(q, k, vt, ld_vt, o, n_rows, nh, mask, err, st);
   return cudaErrorInvalidValue;
 }
 

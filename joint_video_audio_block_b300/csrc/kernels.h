@@ -70,6 +70,9 @@ cudaError_t launch_attention_ref(const bf16* q, const bf16* k, const bf16* vt, i
                                  int hd, cudaStream_t st);
 cudaError_t launch_attention_tc(const bf16* q, const bf16* k, const bf16* vt, int ld_vt, bf16* o, int n_rows, int nh,
                                 int hd, unsigned* err, cudaStream_t st);
+// block-sparse: mask u8 [nh][ceil(n/128)][ceil(n/128)], nonzero = keep (query tile, key tile)
+cudaError_t launch_attention_sparse_tc(const bf16* q, const bf16* k, const bf16* vt, int ld_vt, bf16* o, int n_rows,
+                                       int nh, int hd, const uint8_t* mask, unsigned* err, cudaStream_t st);
 
 int num_sms();
 

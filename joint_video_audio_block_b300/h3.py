@@ -24,7 +24,7 @@ EXPORTS = (
     "h3_workspace_size", "h3_modcache_build", "h3_block_forward", "h3_trunk_forward", "h3_adaln_modulate",
     "h3_linear_forward", "h3_qknorm_rope", "h3_qknorm_rope_static", "h3_attention", "h3_last_device_error",
     "h3_status_str", "h3_kernel_timer_start", "h3_kernel_timer_read", "h3_qkv_project",
-    "h3_qkv_project_workspace_size", "h3_diag_expire_wait",
+    "h3_qkv_project_workspace_size", "h3_diag_expire_wait", "h3_attention_sparse",
 )
 
 # largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
@@ -76,6 +76,7 @@ def lib():
             "h3_qkv_project_workspace_size": (sz, [D, i32]),
             "h3_qkv_project": (i32, [D, LW, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, u32, vp]),
             "h3_attention": (i32, [D, vp, vp, vp, i32, vp, i32, u32, vp]),
+            "h3_attention_sparse": (i32, [D, vp, vp, vp, i32, vp, i32, vp, vp]),
             "h3_last_device_error": (i32, [vp, ctypes.POINTER(u32)]),
             "h3_kernel_timer_start": (i32, [i32]),
             "h3_diag_expire_wait": (i32, [u32, vp]),
@@ -177,6 +178,11 @@ def h3_kernel_timer_read(capacity: int) -> list:
 
 def h3_diag_expire_wait(timeout_us: int, stream):
     _check(lib().h3_diag_expire_wait(timeout_us, stream), "h3_diag_expire_wait")
+
+
+def h3_attention_sparse(dims, q, k, vt, ld_vt, o, n_rows, tile_mask, stream):
+    _check(lib().h3_attention_sparse(ctypes.byref(dims), q, k, vt, ld_vt, o, n_rows, tile_mask, stream),
+           "h3_attention_sparse")
 
 
 def h3_last_device_error(stream):

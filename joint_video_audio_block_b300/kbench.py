@@ -29,14 +29,14 @@ import synth  # noqa: E402
 from joint_video_audio_block_b300 import h3  # noqa: E402
 from joint_video_audio_block_b300 import runtime as R  # noqa: E402
 
-KERNELS = ("attention", "qkv", "o", "fc1", "fc2", "adaln", "qkrope", "qkvrope", "modcache")
+KERNELS = ("attention", "attention_sparse", "qkv", "o", "fc1", "fc2", "adaln", "qkrope", "qkvrope", "modcache")
 
 
 def _normal(shape, std=1.0, mean=0.0, stream=1):
     return synth.device_normal_bf16(7, stream, shape, mean, std)
 
 
-def setup(kernel: str, n: int, int8: bool):
+def setup(kernel: str, n: int, int8: bool, density: float = 0.25):
     """Returns (launch(), flop, bytes, note) for one launch of `kernel` over n rows."""
     d = synth.H3
     H, I, F, hd, nh = d.hidden, d.inner, d.ffn, d.head_dim, d.heads
@@ -54,6 +54,24 @@ def setup(kernel: str, n: int, int8: bool):
             h3.h3_attention(dims, q.data_ptr(), k.data_ptr(), vt.data_ptr(), ld, o.data_ptr(), n, 0, st)
 
         return launch, 4.0 * n * n * I, 4.0 * n * I * 2, "", keep
+
+    if kernel == "attention_sparse":
+        # random (query tile, key tile) mask of the given density; FLOP counted on kept tiles only
+        ld = (n + 63) // 64 * 64
+        nt = (n + 127) // 128
+        q, k = _normal((nh, n, hd), stream=1), _normal((nh, n, hd), stream=2)
+        vt, o = _normal((nh, hd, ld), stream=3), torch.empty(n, I, dtype=torch.bfloat16, device="cuda")
+        mask = (np.random.default_rng(0).random((nh, nt, nt)) < density).astype(np.uint8)
+        rows_in = np.minimum(np.arange(nt) * 128 + 128, n) - np.arange(nt) * 128
+        kept = float((mask * rows_in[None, :, None] * rows_in[None, None, :]).sum())
+        md = torch.from_numpy(mask).cuda()
+        keep += [q, k, vt, o, md]
+
+        def launch():
+            h3.h3_attention_sparse(dims, q.data_ptr(), k.data_ptr(), vt.data_ptr(), ld, o.data_ptr(), n, md.data_ptr(),
+                                   st)
+
+        return launch, 4.0 * kept * hd, 4.0 * n * I * 2, f"tile density {density}: FLOP of kept tiles only", keep
 
     if kernel in ("qkv", "o", "fc1", "fc2"):
         K, n_out, epi = {"qkv": (H, 3 * I, h3.H3_EPI_BIAS), "o": (I, H, h3.H3_EPI_GATE_RES),
@@ -175,9 +193,10 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--int8", action="store_true")
+    ap.add_argument("--density", type=float, default=0.25, help="attention_sparse: fraction of kept tiles")
     a = ap.parse_args(argv)
     torch.cuda.set_device(0)
-    launch, flop, byts, note, _keep = setup(a.kernel, a.rows, a.int8)
+    launch, flop, byts, note, _keep = setup(a.kernel, a.rows, a.int8, a.density)
     for _ in range(a.warmup):
         launch()
     torch.cuda.synchronize()

@@ -268,6 +268,38 @@ def attention(q, k, v, rows=None) -> np.ndarray:
     return out
 
 
+def attention_tile_sparse(q, k, v, tile_mask, tile: int = 128, rows=None) -> np.ndarray:
+    """Block-sparse attention: the unmasked attention above restricted, per head, to the
+    (query tile, key tile) blocks a tile mask keeps -- the video sparse attention form of the
+    "FastH3 OmniRef (Ref2VA) on Apple Silicon MLX" page, section "Opt-in M5 attention backend"
+    (a VSA tile mask selects tiles of 64 or 128 with head dimension 128; there the mask comes
+    from trained gates, here it is given).  Scores outside the kept tiles are -inf; a query row
+    that keeps no tile outputs 0.
+
+    q, k, v: [N, heads, hd]; tile_mask: [heads, ceil(N/tile), ceil(N/tile)], nonzero = keep.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n = q.shape[0]
+    sel = np.arange(n) if rows is None else np.asarray(rows)
+    nh, hd = q.shape[1], q.shape[2]
+    out = np.zeros((len(sel), nh, hd))
+    inv = 1.0 / math.sqrt(hd)
+    key_tile = np.arange(n) // tile
+    for h in range(nh):
+        keep = np.asarray(tile_mask[h], dtype=bool)[(sel // tile)[:, None], key_tile[None, :]]  # [rows, N]
+        s = (q[sel, h, :] @ k[:, h, :].T) * inv
+        s = np.where(keep, s, -np.inf)
+        live = keep.any(axis=1)
+        m = np.where(live, s.max(axis=1), 0.0)
+        p = np.where(keep, np.exp(s - m[:, None]), 0.0)
+        den = p.sum(axis=1)
+        o = (p @ v[:, h, :]) / np.where(live, den, 1.0)[:, None]
+        out[:, h, :] = np.where(live[:, None], o, 0.0)
+    return out
+
+
 # ----------------------------------------------------------------------------------------
 # a1..a8: one block; a10: the trunk
 # ----------------------------------------------------------------------------------------

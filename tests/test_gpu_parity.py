@@ -45,8 +45,11 @@ def check(gpu, ref, rel=REL_L2, abs_=MAX_ABS, what=""):
 def check_step(gpu, ref, what="", spread=2e-3, ulps=1, extra=None):
     """One step with identical bf16 inputs on both sides: the GPU output is the fp32 result
     rounded once to bf16, so each element is within 2^-8 |ref| (one bf16 ulp, covering the
-    half-ulp rounding) plus `spread` x rms(ref) for fp32 accumulation order (and, for attention,
-    the bf16 rounding of the probabilities)."""
+    half-ulp rounding) plus `spread` x rms(ref) for fp32 accumulation order, plus `extra` where
+    a step rounds an intermediate.  Attention rounds each probability to bf16 (relative error
+    <= 2^-9) before P.V while the normaliser keeps the unrounded sum, so its output moves by at
+    most 2^-9 sum_j p_j |v_j| / sum_j p_j: the tests pass that (the oracle's attention of |v|)
+    as `extra`."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     r, m = _err(gpu, ref)
@@ -381,7 +384,65 @@ def test_attention(n, nh, hd, rows, flags):
     sel = np.arange(n) if rows is None else np.random.default_rng(n).choice(n, rows, replace=False)
     t = lambda a: O.widen_bf16(a).transpose(1, 0, 2)  # noqa: E731
     ref = O.attention(t(q), t(k), t(v), rows=sel).reshape(len(sel), nh * hd)
-    check_step(R.f32_from_bf16(o)[sel], ref, what=f"attention n={n} f{flags}", spread=1e-2)
+    p_err = 2.0 ** -9 * O.attention(t(q), t(k), np.abs(t(v)), rows=sel).reshape(len(sel), nh * hd)
+    check_step(R.f32_from_bf16(o)[sel], ref, what=f"attention n={n} f{flags}", spread=1e-3, extra=p_err)
+
+
+def _sparse_case(n, nh, hd, density, seed):
+    q, k, v = _attn_inputs(n, nh, hd, seed=seed)
+    nt = (n + 127) // 128
+    mask = (np.random.default_rng(seed).random((nh, nt, nt)) < density).astype(np.uint8)
+    mask[:, :, 0] |= 1  # most query tiles keep at least the first key tile
+    if nt >= 2:
+        mask[0, 1, :] = 0  # head 0, query tile 1 keeps nothing: zero rows
+        mask[0, 0, :] = 1  # ... while its pair partner keeps everything
+    ld_vt = (n + 63) // 64 * 64
+    vt = np.zeros((nh, hd, ld_vt), np.uint16)
+    vt[:, :, :n] = v.transpose(0, 2, 1)
+    return q, k, v, vt, ld_vt, mask
+
+
+def _run_sparse(n, nh, hd, q, k, vt, ld_vt, mask):
+    o = torch.full((n, nh * hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dims = h3.make_dims(nh * hd, nh, hd, 128, (hd // 8, 3 * hd // 16, 3 * hd // 16))
+    qd, kd, vd = R.bf16_from_bits(q), R.bf16_from_bits(k), R.bf16_from_bits(vt)
+    md = torch.from_numpy(mask).cuda()
+    h3.h3_attention_sparse(dims, qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), ld_vt, o.data_ptr(), n, md.data_ptr(),
+                           h3.stream_ptr())
+    sync_ok()
+    return o, dims, (qd, kd, vd)
+
+
+@pytest.mark.parametrize("n,nh,hd,density,rows", [(300, 3, 128, 0.5, None), (300, 2, 64, 0.5, None),
+                                                  (1829, 8, 128, 0.3, None), (12936, 4, 128, 0.2, 256)])
+def test_attention_sparse(n, nh, hd, density, rows):
+    """Block-sparse attention against the oracle's tile-masked softmax on the same bf16 inputs;
+    rows of a query tile that keeps no key tile must be exactly zero."""
+    q, k, v, vt, ld_vt, mask = _sparse_case(n, nh, hd, density, seed=n + nh)
+    o, _, _ = _run_sparse(n, nh, hd, q, k, vt, ld_vt, mask)
+    sel = np.arange(n) if rows is None else np.sort(np.random.default_rng(n).choice(n, rows, replace=False))
+    t = lambda a: O.widen_bf16(a).transpose(1, 0, 2)  # noqa: E731
+    ref = O.attention_tile_sparse(t(q), t(k), t(v), mask, tile=128, rows=sel).reshape(len(sel), nh * hd)
+    p_err = 2.0 ** -9 * O.attention_tile_sparse(t(q), t(k), np.abs(t(v)), mask, tile=128, rows=sel).reshape(
+        len(sel), nh * hd)
+    got = R.f32_from_bf16(o)[sel]
+    check_step(got, ref, what=f"sparse attention n={n} nh={nh} hd={hd} density={density}", spread=1e-3,
+               extra=p_err)
+    if n > 128:
+        assert np.all(R.f32_from_bf16(o)[128:256, :hd] == 0)  # head 0, query tile 1
+
+
+def test_attention_sparse_all_kept_equals_dense():
+    """With every tile kept the sparse kernel does the dense kernel's arithmetic in the same
+    order: identical bits."""
+    n, nh, hd = 1829, 4, 128
+    q, k, v, vt, ld_vt, _ = _sparse_case(n, nh, hd, 1.0, seed=9)
+    nt = (n + 127) // 128
+    o_s, dims, (qd, kd, vd) = _run_sparse(n, nh, hd, q, k, vt, ld_vt, np.ones((nh, nt, nt), np.uint8))
+    o_d = torch.empty_like(o_s)
+    h3.h3_attention(dims, qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), ld_vt, o_d.data_ptr(), n, 0, h3.stream_ptr())
+    sync_ok()
+    assert torch.equal(o_s, o_d)
 
 
 # ----------------------------------------------------------------------------- block / trunk
@@ -529,6 +590,34 @@ def test_trunk33720_equals_block_sequence():
     assert torch.equal(x_tr, x_seq)
 
 
+def test_trunk_replays_from_a_cuda_graph():
+    """The trunk call holds no host state between launches, so a caller can capture it once
+    in a CUDA graph and replay it: every replay equals an eager call bit for bit."""
+    c = Case("block1829", n_blocks=2)
+    wts = [R.upload_block(w) for w in c.w_bits]
+    bws = [h3.make_block_w(w) for w in wts]
+    ws = R.workspace(c.dims, c.n)
+    x_eager = c.x.clone()
+    args = lambda x: (c.dims, bws, 2, c.table.data_ptr(), c.T, x.data_ptr(), c.n, c.tag_d.data_ptr(),  # noqa: E731
+                      c.tidx_d.data_ptr(), c.pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0)
+    h3.h3_trunk_forward(*args(x_eager), h3.stream_ptr())  # also the warm-up before capture
+    sync_ok()
+    x_g = torch.empty_like(c.x)
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            h3.h3_trunk_forward(*args(x_g), h3.stream_ptr(side))
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        x_g.copy_(c.x)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(x_g, x_eager)
+    sync_ok()
+
+
 def test_trunk_equals_block_sequence():
     c = Case("block1829", n_blocks=3)
     wts = [R.upload_block(w) for w in c.w_bits]
@@ -579,7 +668,8 @@ def test_bounded_wait_expires_and_context_survives():
     sync_ok()
     t = lambda a: O.widen_bf16(a).transpose(1, 0, 2)  # noqa: E731
     ref = O.attention(t(q), t(k), t(v)).reshape(n, nh * hd)
-    check_step(R.f32_from_bf16(o), ref, what="attention after an expired wait", spread=1e-2)
+    p_err = 2.0 ** -9 * O.attention(t(q), t(k), np.abs(t(v))).reshape(n, nh * hd)
+    check_step(R.f32_from_bf16(o), ref, what="attention after an expired wait", spread=1e-3, extra=p_err)
 
 
 def test_zero_rows_and_bad_arguments():

@@ -402,3 +402,61 @@ def test_flop_model_matches_linear_share_on_the_pages():
     for n, share in zip(g["rows"], g["value"]):
         lin, att = O.block_flops(synth.H3, n)
         assert abs(lin / (lin + att) - share) <= g["tolerance"], (n, lin / (lin + att))
+
+
+# ----------------------------------------------------------------------------- block-sparse attention
+
+
+def _qkv(n, nh, hd, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((n, nh, hd)), rng.standard_normal((n, nh, hd)), rng.standard_normal((n, nh, hd)))
+
+
+def test_sparse_attention_all_kept_is_dense():
+    q, k, v = _qkv(37, 2, 8, 1)
+    nt = -(-37 // 8)
+    full = np.ones((2, nt, nt), np.uint8)
+    np.testing.assert_allclose(O.attention_tile_sparse(q, k, v, full, tile=8), O.attention(q, k, v), rtol=0, atol=1e-13)
+
+
+def test_sparse_attention_single_tile_is_attention_over_that_tile():
+    """Keeping one key tile is plain attention over just those keys (computed by slicing)."""
+    q, k, v = _qkv(40, 1, 4, 2)
+    mask = np.zeros((1, 5, 5), np.uint8)
+    mask[0, :, 3] = 1  # every query tile keeps key tile 3 = keys 24..31
+    got = O.attention_tile_sparse(q, k, v, mask, tile=8)
+    # brute force with explicit loops over the kept keys
+    ref = np.zeros_like(q)
+    for r in range(40):
+        s = np.array([q[r, 0] @ k[j, 0] for j in range(24, 32)]) / 2.0
+        p = np.exp(s - s.max())
+        ref[r, 0] = (p[:, None] * v[24:32, 0]).sum(0) / p.sum()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_sparse_attention_row_without_kept_tiles_is_zero():
+    q, k, v = _qkv(24, 1, 4, 3)
+    mask = np.ones((1, 3, 3), np.uint8)
+    mask[0, 1, :] = 0  # query tile 1 (rows 8..15) keeps nothing
+    got = O.attention_tile_sparse(q, k, v, mask, tile=8)
+    assert np.all(got[8:16] == 0)
+    np.testing.assert_allclose(got[:8], O.attention(q, k, v)[:8], rtol=0, atol=1e-13)
+
+
+def test_sparse_attention_tiny_brute_force():
+    """Exhaustive loop over a random mask: each row's softmax over exactly its kept keys."""
+    rng = np.random.default_rng(4)
+    n, nh, hd, tile = 12, 2, 3, 4
+    q, k, v = _qkv(n, nh, hd, 5)
+    mask = (rng.random((nh, 3, 3)) < 0.5).astype(np.uint8)
+    got = O.attention_tile_sparse(q, k, v, mask, tile=tile)
+    for h in range(nh):
+        for r in range(n):
+            keys = [j for j in range(n) if mask[h, r // tile, j // tile]]
+            if not keys:
+                assert np.all(got[r, h] == 0)
+                continue
+            s = np.array([q[r, h] @ k[j, h] for j in keys]) / math.sqrt(hd)
+            p = np.exp(s - s.max())
+            ref = sum(p[i] * v[j, h] for i, j in enumerate(keys)) / p.sum()
+            np.testing.assert_allclose(got[r, h], ref, rtol=0, atol=1e-12)
