@@ -118,6 +118,42 @@ h3_status h3_trunk_forward(const h3_dims* dims, const h3_block_w* blocks, int n_
                            void* x, int n_rows, const uint8_t* tag, const int32_t* tidx, const float* pos,
                            void* workspace, size_t ws_bytes, unsigned flags, void* stream);
 
+/* ---- trunk entry and exit, and the sampler ("minimax-h3-mlx" README, "Architecture": two
+ * input patch projections and two output heads around the trunk; "Porting notes": those ship
+ * as float32 tensors; "Layout": rectified-flow Euler with an exponential sigma shift) ---- */
+
+/* x_rows[r] = bf16(W z[r] + b), r < n_rows, float32 weights and arithmetic: the input
+ * projection of one modality's rows (video or condition latents: K = 96 patch features;
+ * audio: K = 32).  z: device f32 [n_rows, K]; w: device f32 [H, K] (checkpoint orientation);
+ * b: device f32 [H] or NULL; x_rows: device bf16, the first of the modality's n_rows rows of
+ * the packed hidden stream [N, H] (16-byte aligned).  Text rows enter through a bf16 linear
+ * (h3_linear_forward, condition_proj [H, 5120]). */
+h3_status h3_embed_rows(const h3_dims* dims, const float* z, int K, const float* w, const float* b, int n_rows,
+                        void* x_rows, void* stream);
+
+/* Final-layer modulation table: table_f[t][j] = bf16(sum_k w[j][k] temb[t][k] + b[j]),
+ * j < 6H, read as 3 modality tags x (shift, scale) x H.  temb: device f32 [T, Dt]; w: device
+ * bf16 [6H, Dt] (16-byte aligned); b: device bf16 [6H] or NULL; table_f: device bf16 [T][6H]. */
+h3_status h3_final_modcache_build(const h3_dims* dims, const float* temb, int T, int Dt, const void* w, const void* b,
+                                  void* table_f, void* stream);
+
+/* Output head of one modality's rows, in float32:
+ *   v[r] = W (LN(x[r]) (1 + scale) + shift) + b,  (shift, scale) = table_f[tidx[r]*t_stride + (2 tag[r] + {0,1}) H]
+ * and, when z_inout is given, the Euler transition z[r] += dsigma * v[r] (dsigma = sigma_next -
+ * sigma_now of the modality's schedule).  x_rows: device bf16 [n_rows, H] (16-byte aligned);
+ * tag, tidx: device, of these rows; table_f: device bf16 (t_stride >= 6H); w: device f32
+ * [K_out, H]; b: device f32 [K_out] or NULL; v_out: device f32 [n_rows, K_out] or NULL;
+ * z_inout: device f32 [n_rows, K_out] or NULL (not both NULL).  K_out <= 128. */
+h3_status h3_head_forward(const h3_dims* dims, const void* x_rows, int n_rows, const uint8_t* tag, const int32_t* tidx,
+                          const void* table_f, long long t_stride, const float* w, const float* b, int K_out,
+                          float* v_out, float* z_inout, float dsigma, void* stream);
+
+/* HOST: the sampling grid of one schedule, steps + 1 values from 1 to 0: a float32 linspace
+ * (float32 step; first half start + step*i, second half end - step*(n-1-i), each one fused
+ * multiply-add) followed by the time shift s sigma / (1 + (s - 1) sigma) in float32.
+ * sigma_out: host f32 [steps + 1]. */
+h3_status h3_sigma_schedule(int steps, float shift, float* sigma_out);
+
 /* ---- step entry points (each row of the block on its own; used for per-step parity) ---- */
 
 /* a1 / a6 -- gather + LayerNorm + modulate ("minimax-h3-mlx" README, "AdaLN: measure, do not

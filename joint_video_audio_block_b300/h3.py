@@ -24,7 +24,8 @@ EXPORTS = (
     "h3_workspace_size", "h3_modcache_build", "h3_block_forward", "h3_trunk_forward", "h3_adaln_modulate",
     "h3_linear_forward", "h3_qknorm_rope", "h3_qknorm_rope_static", "h3_attention", "h3_last_device_error",
     "h3_status_str", "h3_kernel_timer_start", "h3_kernel_timer_read", "h3_qkv_project",
-    "h3_qkv_project_workspace_size", "h3_diag_expire_wait", "h3_attention_sparse",
+    "h3_qkv_project_workspace_size", "h3_diag_expire_wait", "h3_attention_sparse", "h3_embed_rows",
+    "h3_final_modcache_build", "h3_head_forward", "h3_sigma_schedule",
 )
 
 # largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
@@ -77,6 +78,10 @@ def lib():
             "h3_qkv_project": (i32, [D, LW, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, u32, vp]),
             "h3_attention": (i32, [D, vp, vp, vp, i32, vp, i32, u32, vp]),
             "h3_attention_sparse": (i32, [D, vp, vp, vp, i32, vp, i32, vp, vp]),
+            "h3_embed_rows": (i32, [D, vp, i32, vp, vp, i32, vp, vp]),
+            "h3_final_modcache_build": (i32, [D, vp, i32, i32, vp, vp, vp, vp]),
+            "h3_head_forward": (i32, [D, vp, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp, ctypes.c_float, vp]),
+            "h3_sigma_schedule": (i32, [i32, ctypes.c_float, ctypes.POINTER(ctypes.c_float)]),
             "h3_last_device_error": (i32, [vp, ctypes.POINTER(u32)]),
             "h3_kernel_timer_start": (i32, [i32]),
             "h3_diag_expire_wait": (i32, [u32, vp]),
@@ -183,6 +188,27 @@ def h3_diag_expire_wait(timeout_us: int, stream):
 def h3_attention_sparse(dims, q, k, vt, ld_vt, o, n_rows, tile_mask, stream):
     _check(lib().h3_attention_sparse(ctypes.byref(dims), q, k, vt, ld_vt, o, n_rows, tile_mask, stream),
            "h3_attention_sparse")
+
+
+def h3_embed_rows(dims, z, K, w, b, n_rows, x_rows, stream):
+    _check(lib().h3_embed_rows(ctypes.byref(dims), z, K, w, b, n_rows, x_rows, stream), "h3_embed_rows")
+
+
+def h3_final_modcache_build(dims, temb, T, Dt, w, b, table_f, stream):
+    _check(lib().h3_final_modcache_build(ctypes.byref(dims), temb, T, Dt, w, b, table_f, stream),
+           "h3_final_modcache_build")
+
+
+def h3_head_forward(dims, x_rows, n_rows, tag, tidx, table_f, t_stride, w, b, K_out, v_out, z_inout, dsigma, stream):
+    _check(lib().h3_head_forward(ctypes.byref(dims), x_rows, n_rows, tag, tidx, table_f, t_stride, w, b, K_out, v_out,
+                                 z_inout, dsigma, stream), "h3_head_forward")
+
+
+def h3_sigma_schedule(steps: int, shift: float) -> list:
+    """Host-side sampling grid (steps + 1 float32 values from 1 to 0) of one shifted schedule."""
+    buf = (ctypes.c_float * (steps + 1))()
+    _check(lib().h3_sigma_schedule(steps, shift, buf), "h3_sigma_schedule")
+    return [buf[i] for i in range(steps + 1)]
 
 
 def h3_last_device_error(stream):

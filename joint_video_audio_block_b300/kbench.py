@@ -29,7 +29,8 @@ import synth  # noqa: E402
 from joint_video_audio_block_b300 import h3  # noqa: E402
 from joint_video_audio_block_b300 import runtime as R  # noqa: E402
 
-KERNELS = ("attention", "attention_sparse", "qkv", "o", "fc1", "fc2", "adaln", "qkrope", "qkvrope", "modcache")
+KERNELS = ("block", "attention", "attention_sparse", "qkv", "o", "fc1", "fc2", "adaln", "qkrope", "qkvrope",
+           "modcache", "embed", "head")
 
 
 def _normal(shape, std=1.0, mean=0.0, stream=1):
@@ -43,6 +44,31 @@ def setup(kernel: str, n: int, int8: bool, density: float = 0.25):
     dims = R.dims_of(d)
     st = h3.stream_ptr()
     keep = []
+
+    if kernel == "block":
+        # one whole DiT block (h3_block_forward: a1..a8) on the packed layout of the nearest
+        # configuration; FLOP = the MMA work of the block (linears + attention)
+        cfg = min(synth.CONFIGS.values(), key=lambda c: abs(c.layout.n_rows - n) if c.dims is d else 1 << 30)
+        tag, tidx, pos = (np.resize(a, (n,) + a.shape[1:]) for a in synth.packed_rows(cfg))
+        w = synth.device_block_weights(synth.CONFIGS["block12936"], 0)
+        if int8:
+            raise ValueError("block timing is bf16 only")
+        bw = h3.make_block_w(w)
+        x = _normal((n, H), stream=30)
+        out = torch.empty_like(x)
+        table = _normal((1, 18 * H), 0.5, stream=31)
+        tag_d = torch.from_numpy(np.ascontiguousarray(tag)).cuda()
+        tidx_d = torch.zeros(n, dtype=torch.int32, device="cuda")
+        pos_d = torch.from_numpy(np.ascontiguousarray(pos)).cuda()
+        ws = R.workspace(dims, n)
+        keep += [w, bw, x, out, table, tag_d, tidx_d, pos_d, ws]
+
+        def launch():
+            h3.h3_block_forward(dims, bw, table.data_ptr(), 18 * H, 1, x.data_ptr(), out.data_ptr(), n, tag_d.data_ptr(),
+                                tidx_d.data_ptr(), pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0, st)
+
+        lin = 2.0 * n * (3 * I * H + H * I + 2 * F * H + H * F)
+        return launch, lin + 4.0 * n * n * I, 0.0, f"packed layout of {cfg.name}; FLOP = linears + attention", keep
 
     if kernel == "attention":
         ld = (n + 63) // 64 * 64
@@ -168,6 +194,34 @@ def setup(kernel: str, n: int, int8: bool, density: float = 0.25):
 
         byts = n * H * 2.0 + 3 * I * H * wbytes + 3.0 * n * I * 2 + n * hd * 4.0
         return launch, 2.0 * n * H * 3 * I, byts, "includes the per-row cos/sin table kernel", keep
+
+    if kernel in ("embed", "head"):
+        # video-latent rows: the input patch projection (96 -> H) or the final AdaLN + output head
+        # (H -> 96) with the Euler update of the float32 latents, float32 weights
+        K = synth.VIDEO_FEATURES
+        f32 = lambda shape, s_, std=1.0: torch.randn(shape, generator=torch.Generator("cuda").manual_seed(s_),  # noqa
+                                                     device="cuda") * std
+        x = _normal((n, H), stream=40)
+        z = f32((n, K), 41)
+        if kernel == "embed":
+            w, b = f32((H, K), 42, 0.02), f32((H,), 43, 0.02)
+            keep += [x, z, w, b]
+
+            def launch():
+                h3.h3_embed_rows(dims, z.data_ptr(), K, w.data_ptr(), b.data_ptr(), n, x.data_ptr(), st)
+
+            return launch, 2.0 * n * H * K, n * K * 4.0 + H * K * 4.0 + n * H * 2.0, "float32 CUDA-core", keep
+        w, b = f32((K, H), 44, 0.02), f32((K,), 45, 0.02)
+        table = _normal((1, 6 * H), 0.5, stream=46)
+        tag_d = torch.full((n,), 2, dtype=torch.uint8, device="cuda")
+        tidx_d = torch.zeros(n, dtype=torch.int32, device="cuda")
+        keep += [x, z, w, b, table, tag_d, tidx_d]
+
+        def launch():
+            h3.h3_head_forward(dims, x.data_ptr(), n, tag_d.data_ptr(), tidx_d.data_ptr(), table.data_ptr(), 6 * H,
+                               w.data_ptr(), b.data_ptr(), K, None, z.data_ptr(), -0.01, st)
+
+        return launch, 2.0 * n * H * K, n * H * 2.0 + 2 * n * K * 4.0, "float32 CUDA-core; with the Euler update", keep
 
     if kernel == "modcache":
         T = n

@@ -377,6 +377,83 @@ def trunk_forward(x, block_weight_list, table_bf16, tag, tidx, pos, dims, *, emu
 
 
 # ----------------------------------------------------------------------------------------
+# trunk entry and exit; the sampler
+# ----------------------------------------------------------------------------------------
+
+
+def embed_rows(z, w, b) -> np.ndarray:
+    """Input projection of one modality's rows into the hidden stream: x = z W^T + b.
+
+    minimax-h3-mlx README, "Architecture": modality-specific behaviour comes only from the two
+    input patch projections (video, audio), the per-row tag and the two output heads; the
+    conditioner's hidden state enters through condition_proj (section "Encoder truncation").
+    "Porting notes" / "Validation": the patch projections ship as float32 tensors, so the
+    projection is float32 weights on float32 latents; the result joins the bf16 hidden stream.
+    z: [rows, K]; w: [H, K] float32; b: [H].  Returns float64 (the exact value).
+    """
+    return linear(np.asarray(z, dtype=np.float64), np.asarray(w, dtype=np.float64), b)
+
+
+def final_modulation(table_f, tag, tidx, m: int, hidden: int) -> np.ndarray:
+    """Per-row final-layer modulation: table_f[tidx[r], 2*tag[r] + m, :] with m = 0 shift, 1 scale.
+
+    Reading: the timestep-aware output head ("H3-metal" README, "Sampler and DiT controls":
+    the patch projection and timestep-aware head stay fresh) is an AdaLN with its own two
+    tensors per modality tag, tabulated from the timestep embedding like the blocks' six.
+    table_f: [T, 6H]."""
+    tf = np.asarray(table_f, dtype=np.float64).reshape(table_f.shape[0], 6, hidden)
+    return tf[np.asarray(tidx, np.int64), 2 * np.asarray(tag, np.int64) + m, :]
+
+
+def head_forward(x, shift, scale, w, b, eps: float) -> np.ndarray:
+    """Output head of one modality's rows: v = (LN(x)(1 + scale) + shift) W^T + b.
+
+    minimax-h3-mlx README, "Architecture": two output heads; "Porting notes": they ship as
+    float32 tensors ("H3-metal" README, "Specialized projection kernels": the close-reference
+    head keeps them in F32).  x: bf16 values [rows, H]; w: [K_out, H] float32."""
+    xn = adaln_modulate(np.asarray(x, dtype=np.float64), shift, scale, eps)
+    return linear(xn, np.asarray(w, dtype=np.float64), b)
+
+
+def linspace_f32(start: float, end: float, steps: int) -> np.ndarray:
+    """torch.linspace in float32 as the minimax-h3-mlx README ("Porting notes", "Validation")
+    describes ATen's: a float32 step (end - start) / (steps - 1); the first half evaluated as
+    start + step * i, the second half as end - step * (steps - 1 - i), each with one fused
+    multiply-add rounded to float32.  (The fused result equals rounding the exact float64
+    value of the product-sum once, since step and i are exact and the float64 product of a
+    24-bit and a <= 24-bit integer is exact.)"""
+    f32 = np.float32
+    if steps == 1:
+        return np.array([start], np.float32)
+    step = f32((f32(end) - f32(start)) / f32(steps - 1))
+    half = steps // 2
+    out = np.empty(steps, np.float32)
+    for i in range(steps):
+        if i < half:
+            out[i] = f32(np.float64(f32(start)) + np.float64(step) * i)
+        else:
+            out[i] = f32(np.float64(f32(end)) - np.float64(step) * (steps - 1 - i))
+    return out
+
+
+def shifted_sigmas(steps: int, shift: float) -> np.ndarray:
+    """Rectified-flow sampling grid for `steps` Euler transitions: sigma_i from 1 to 0 on the
+    float32 linspace grid, then the time shift sigma' = s sigma / (1 + (s - 1) sigma) in float32
+    (minimax-h3-mlx README, "AdaLN precompute": separate video and audio shifts, 12.0 and 3.0;
+    "Porting notes": scheduler scalars in float32).  Returns float32 [steps + 1]."""
+    f32 = np.float32
+    sig = linspace_f32(1.0, 0.0, steps + 1)
+    s = f32(shift)
+    return (s * sig / (f32(1.0) + (s - f32(1.0)) * sig)).astype(np.float32)
+
+
+def euler_step(z, v, sigma_now: float, sigma_next: float) -> np.ndarray:
+    """One rectified-flow Euler transition: z <- z + (sigma_next - sigma_now) v
+    (minimax-h3-mlx README, "Layout": the scheduler is rectified-flow Euler)."""
+    return np.asarray(z, dtype=np.float64) + (float(sigma_next) - float(sigma_now)) * np.asarray(v, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------------------
 # work model
 # ----------------------------------------------------------------------------------------
 

@@ -324,6 +324,37 @@ def adaln_weights(cfg: Config, block: int = 0) -> tuple:
     return W, b
 
 
+# trunk entry / exit: latent feature widths (video: 24 latent channels x a 1x2x2 patch; audio:
+# 32 latent channels) and the condition-encoder width
+VIDEO_FEATURES, AUDIO_FEATURES, TEXT_FEATURES = 96, 32, 5120
+_T_PV, _T_PVB, _T_PA, _T_PAB, _T_HV, _T_HVB, _T_HA, _T_HAB, _T_FW, _T_FB, _T_ZV, _T_ZA = range(40, 52)
+
+
+def io_weights(cfg: Config) -> dict:
+    """Trunk entry / exit weights: float32 patch projections [H, K] and output heads [K, H]
+    with float32 biases, N(0, 0.02); the final AdaLN projection [6H, Dt] (bf16 bits) and bias."""
+    d = cfg.dims
+    H, s = d.hidden, cfg.seed
+    f = lambda t, shape: normal_f32(s, _stream(0xFFFE, t), shape, 0.0, 0.02)  # noqa: E731
+    return {
+        "patch_v": f(_T_PV, (H, VIDEO_FEATURES)), "patch_v_b": f(_T_PVB, (H,)),
+        "patch_a": f(_T_PA, (H, AUDIO_FEATURES)), "patch_a_b": f(_T_PAB, (H,)),
+        "head_v": f(_T_HV, (VIDEO_FEATURES, H)), "head_v_b": f(_T_HVB, (VIDEO_FEATURES,)),
+        "head_a": f(_T_HA, (AUDIO_FEATURES, H)), "head_a_b": f(_T_HAB, (AUDIO_FEATURES,)),
+        "final_w": normal_bf16(s, _stream(0xFFFE, _T_FW), (6 * H, d.temb_dim), 0.0, 0.02),
+        "final_b": normal_bf16(s, _stream(0xFFFE, _T_FB), (6 * H,), 0.0, 0.02),
+    }
+
+
+def latents(cfg: Config):
+    """Noisy latent rows of the video (and condition) rows and of the audio rows, N(0, 1) float32."""
+    lay = cfg.layout
+    s = cfg.seed
+    zv = normal_f32(s, _stream(0xFFFE, _T_ZV), (lay.n_cond + lay.n_video, VIDEO_FEATURES))
+    za = normal_f32(s, _stream(0xFFFE, _T_ZA), (lay.audio, AUDIO_FEATURES))
+    return zv, za
+
+
 def temb(cfg: Config) -> np.ndarray:
     return sinusoidal_temb(cfg.timesteps[: cfg.n_timesteps], cfg.dims.temb_dim)
 

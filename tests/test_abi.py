@@ -92,3 +92,15 @@ def test_invalid_arguments_rejected_before_launch(h3mod):
     assert st == h3mod.H3_EINVAL
     st = L.h3_attention(ctypes.byref(d), None, None, None, 72, None, 72, 0, None)
     assert st == h3mod.H3_EINVAL
+
+
+def test_sigma_schedule_is_the_oracle_grid(h3mod):
+    """Host-only entry point (no GPU): the library's sampling grid equals the oracle's float32
+    linspace + time shift bit for bit."""
+    import numpy as np
+
+    import oracle.h3_oracle as O
+
+    for steps, shift in ((40, 12.0), (40, 3.0), (8, 12.0), (77, 1.0), (1, 3.0)):
+        got = np.asarray(h3mod.h3_sigma_schedule(steps, shift), np.float32)
+        np.testing.assert_array_equal(got, O.shifted_sigmas(steps, shift))

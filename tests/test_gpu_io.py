@@ -1,0 +1,138 @@
+"""GPU parity of the trunk's entry and exit and of the sampler's Euler transition, through the
+C ABI against the CPU oracle on the same seeded inputs.
+
+All three are float32 arithmetic on the GPU (float32 weights, as the released checkpoint ships
+the patch projections and output heads).  Bounds: the bf16 output of the input projection is
+within one bf16 ulp of the exact value plus the float32 accumulation bound K 2^-24 sum|w z|; the
+float32 head output is within the float32 accumulation bound H 2^-24 sum|w xn| plus the
+LayerNorm's own float32 error (the same bound again, generously); the Euler update adds its
+own rounding of z."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import oracle.h3_oracle as O  # noqa: E402
+import synth  # noqa: E402
+from joint_video_audio_block_b300 import h3, runtime as R  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _sync():
+    torch.cuda.synchronize()
+    st, site = h3.h3_last_device_error(h3.stream_ptr())
+    assert st == h3.H3_OK, f"device error {site:#x}"
+
+
+def _segments(cfg):
+    """(first row, rows) of the video-latent rows (conditions + video) and of the audio rows."""
+    lay = cfg.layout
+    cond0 = lay.text
+    audio0 = cond0 + lay.n_cond
+    video0 = audio0 + lay.audio
+    return (cond0, lay.n_cond, video0, lay.n_video), (audio0, lay.audio)
+
+
+@pytest.mark.parametrize("name", ["tiny", "block1829", "trunk33720"])
+def test_embed_rows(name):
+    cfg = synth.CONFIGS[name]
+    d, n = cfg.dims, cfg.layout.n_rows
+    H = d.hidden
+    dims = R.dims_of(d)
+    w = synth.io_weights(cfg)
+    zv, za = synth.latents(cfg)
+    (c0, nc, v0, nv), (a0, na) = _segments(cfg)
+    x = torch.full((n, H), 7.0, dtype=torch.bfloat16, device="cuda")  # sentinel
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    pv, pvb, pa, pab = dev(w["patch_v"]), dev(w["patch_v_b"]), dev(w["patch_a"]), dev(w["patch_a_b"])
+    zv_d, za_d = dev(zv), dev(za)
+    st = h3.stream_ptr()
+    row = lambda r: x.data_ptr() + r * H * 2  # noqa: E731
+    if nc:
+        h3.h3_embed_rows(dims, zv_d.data_ptr(), synth.VIDEO_FEATURES, pv.data_ptr(), pvb.data_ptr(), nc, row(c0), st)
+    h3.h3_embed_rows(dims, zv_d[nc:].data_ptr(), synth.VIDEO_FEATURES, pv.data_ptr(), pvb.data_ptr(), nv, row(v0), st)
+    h3.h3_embed_rows(dims, za_d.data_ptr(), synth.AUDIO_FEATURES, pa.data_ptr(), pab.data_ptr(), na, row(a0), st)
+    _sync()
+    got = R.f32_from_bf16(x).astype(np.float64)
+    assert np.all(got[:c0] == 7.0)  # text rows untouched
+    for z, W, b, r0, rows in ((zv[:nc], w["patch_v"], w["patch_v_b"], c0, nc), (zv[nc:], w["patch_v"], w["patch_v_b"], v0, nv),
+                              (za, w["patch_a"], w["patch_a_b"], a0, na)):
+        if rows == 0:
+            continue
+        ref = O.embed_rows(z, W, b)
+        absum = np.abs(z.astype(np.float64)) @ np.abs(W.astype(np.float64)).T + np.abs(b.astype(np.float64))
+        bound = 2.0 ** -8 * np.abs(ref) + z.shape[1] * 2.0 ** -24 * absum
+        err = np.abs(got[r0:r0 + rows] - ref)
+        assert np.all(err <= bound), f"{name} rows {r0}+{rows}: excess {np.max(err - bound):.3e}"
+
+
+def _final_table(cfg):
+    w = synth.io_weights(cfg)
+    temb = synth.temb(cfg)
+    t64, tbf = O.modcache(temb, [w["final_w"]], [w["final_b"]])
+    return w, temb, t64[:, 0, :], tbf[:, 0, :]
+
+
+@pytest.mark.parametrize("name", ["tiny", "trunk33720"])
+def test_final_modcache_build(name):
+    cfg = synth.CONFIGS[name]
+    d = cfg.dims
+    w, temb, t64, tbf = _final_table(cfg)
+    T = t64.shape[0]
+    table = torch.empty(T, 6 * d.hidden, dtype=torch.bfloat16, device="cuda")
+    temb_d, w_d, b_d = torch.from_numpy(temb).cuda(), R.bf16_from_bits(w["final_w"]), R.bf16_from_bits(w["final_b"])
+    h3.h3_final_modcache_build(R.dims_of(d), temb_d.data_ptr(), T, d.temb_dim, w_d.data_ptr(), b_d.data_ptr(),
+                               table.data_ptr(), h3.stream_ptr())
+    _sync()
+    got = R.f32_from_bf16(table).astype(np.float64)
+    absum = np.abs(temb.astype(np.float64)) @ np.abs(O.widen_bf16(w["final_w"])).T + np.abs(O.widen_bf16(w["final_b"]))
+    excess = np.abs(got - t64) - (2.0 ** -8 * np.abs(t64) + 2.0 ** -20 * absum)
+    assert np.all(excess <= 0), excess.max()
+
+
+@pytest.mark.parametrize("name", ["tiny", "block1829", "trunk33720"])
+@pytest.mark.parametrize("modality", ["video", "audio"])
+def test_head_forward_and_euler(name, modality):
+    cfg = synth.CONFIGS[name]
+    d, n = cfg.dims, cfg.layout.n_rows
+    H = d.hidden
+    dims = R.dims_of(d)
+    w, _, _, tbf = _final_table(cfg)
+    (c0, nc, v0, nv), (a0, na) = _segments(cfg)
+    r0, rows = (v0, nv) if modality == "video" else (a0, na)
+    K = synth.VIDEO_FEATURES if modality == "video" else synth.AUDIO_FEATURES
+    W, b = w["head_v" if modality == "video" else "head_a"], w["head_v_b" if modality == "video" else "head_a_b"]
+    x_bits = synth.activations(cfg)[r0:r0 + rows]
+    tag, tidx, _ = synth.packed_rows(cfg, step=3)
+    tag, tidx = tag[r0:r0 + rows], tidx[r0:r0 + rows]
+    T = tbf.shape[0]
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    x = R.bf16_from_bits(x_bits)
+    table = R.bf16_from_bits(O.to_bf16_bits(tbf))
+    Wd, bd, tag_d, tidx_d = dev(W), dev(b), dev(tag), dev(tidx)
+    z0 = synth.normal_f32(cfg.seed, 0xBEEF, (rows, K))
+    z = dev(z0)
+    v = torch.empty(rows, K, dtype=torch.float32, device="cuda")
+    sig = O.shifted_sigmas(40, 12.0 if modality == "video" else 3.0)
+    dsig = float(np.float32(sig[4]) - np.float32(sig[3]))
+    h3.h3_head_forward(dims, x.data_ptr(), rows, tag_d.data_ptr(), tidx_d.data_ptr(), table.data_ptr(), 6 * H,
+                       Wd.data_ptr(), bd.data_ptr(), K, v.data_ptr(), z.data_ptr(), dsig, h3.stream_ptr())
+    _sync()
+    assert T >= 1
+    shift = O.final_modulation(tbf, tag, tidx, 0, H)
+    scale = O.final_modulation(tbf, tag, tidx, 1, H)
+    ref = O.head_forward(O.widen_bf16(x_bits), shift, scale, W, b, d.ln_eps)
+    xn = O.adaln_modulate(O.widen_bf16(x_bits), shift, scale, d.ln_eps)
+    absum = np.abs(xn) @ np.abs(W.astype(np.float64)).T + np.abs(b.astype(np.float64))
+    bound = 2 * H * 2.0 ** -24 * absum
+    got_v = v.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got_v - ref) <= bound), f"head: excess {np.max(np.abs(got_v - ref) - bound):.3e}"
+    rel = np.linalg.norm(got_v - ref) / np.linalg.norm(ref)
+    print(f"head {name} {modality}: rel_l2={rel:.3e}")
+    z_ref = O.euler_step(z0, ref, 0.0, dsig)
+    bound_z = abs(dsig) * bound + 2.0 ** -24 * np.abs(z_ref) * 2
+    assert np.all(np.abs(z.cpu().numpy() - z_ref) <= bound_z)

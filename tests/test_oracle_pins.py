@@ -460,3 +460,71 @@ def test_sparse_attention_tiny_brute_force():
             p = np.exp(s - s.max())
             ref = sum(p[i] * v[j, h] for i, j in enumerate(keys)) / p.sum()
             np.testing.assert_allclose(got[r, h], ref, rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- trunk entry / exit, sampler
+
+
+def test_embed_rows_selector_weights_copy_the_latent():
+    """A 0/1 selector W (column c reads latent feature c mod K) turns the projection into a copy."""
+    rng = np.random.default_rng(6)
+    z = rng.standard_normal((5, 12)).astype(np.float32)
+    H = 40
+    w = np.zeros((H, 12), np.float32)
+    w[np.arange(H), np.arange(H) % 12] = 1.0
+    b = rng.standard_normal(H).astype(np.float32)
+    got = O.embed_rows(z, w, b)
+    np.testing.assert_array_equal(got, z[:, np.arange(H) % 12].astype(np.float64) + b.astype(np.float64))
+
+
+def test_head_on_constant_rows_is_the_projected_shift():
+    """A constant row normalises to zero, so the head's output is W shift + b exactly."""
+    H, K = 64, 6
+    rng = np.random.default_rng(7)
+    x = np.full((3, H), 0.625)
+    shift = rng.standard_normal((3, H))
+    scale = rng.standard_normal((3, H))
+    w = rng.standard_normal((K, H)).astype(np.float32)
+    b = rng.standard_normal(K).astype(np.float32)
+    np.testing.assert_allclose(O.head_forward(x, shift, scale, w, b, 1e-6),
+                               shift @ w.astype(np.float64).T + b, rtol=0, atol=1e-12)
+
+
+def test_final_modulation_indexing():
+    T, H = 3, 8
+    tf = np.arange(T * 6 * H, dtype=np.float64).reshape(T, 6 * H)
+    tag = np.array([0, 1, 2, 2])
+    tidx = np.array([2, 0, 1, 2])
+    for m in (0, 1):
+        got = O.final_modulation(tf, tag, tidx, m, H)
+        for r in range(4):
+            np.testing.assert_array_equal(got[r], tf[tidx[r], (2 * tag[r] + m) * H:(2 * tag[r] + m + 1) * H])
+
+
+@pytest.mark.parametrize("steps", [2, 7, 8, 20, 40, 41, 50, 77])
+def test_linspace_matches_aten(steps):
+    """The pages name ATen's float32 linspace as the grid the scheduler must reproduce."""
+    torch = pytest.importorskip("torch")
+    ref = torch.linspace(1.0, 0.0, steps, dtype=torch.float32).numpy()
+    np.testing.assert_array_equal(O.linspace_f32(1.0, 0.0, steps), ref)
+
+
+def test_shifted_sigmas_endpoints_monotone_and_identity_shift():
+    for shift in (1.0, 3.0, 12.0):
+        s = O.shifted_sigmas(40, shift)
+        assert s[0] == 1.0 and s[-1] == 0.0 and np.all(np.diff(s) < 0)
+    np.testing.assert_array_equal(O.shifted_sigmas(40, 1.0), O.linspace_f32(1.0, 0.0, 41))
+    # a larger shift keeps more of the grid at high noise
+    assert np.all(O.shifted_sigmas(40, 12.0)[1:-1] > O.shifted_sigmas(40, 3.0)[1:-1])
+
+
+def test_euler_integrates_a_constant_velocity_exactly():
+    rng = np.random.default_rng(8)
+    z0 = rng.standard_normal(10)
+    v = rng.standard_normal(10)
+    sig = O.shifted_sigmas(20, 12.0).astype(np.float64)
+    z = z0
+    for i in range(20):
+        z = O.euler_step(z, v, sig[i], sig[i + 1])
+    np.testing.assert_allclose(z, z0 + (sig[-1] - sig[0]) * v, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(O.euler_step(z0, v, 0.5, 0.5), z0)
