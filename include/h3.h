@@ -154,6 +154,32 @@ h3_status h3_head_forward(const h3_dims* dims, const void* x_rows, int n_rows, c
  * sigma_out: host f32 [steps + 1]. */
 h3_status h3_sigma_schedule(int steps, float shift, float* sigma_out);
 
+/* One denoiser transition of the sampler over the packed sequence [text | cond | audio | video]:
+ *   x[text rows]  = text_x (the projected conditioner rows, computed once by the caller)
+ *   x[cond rows]  = embed(z_cond; patch_v),  x[audio rows] = embed(z_audio; patch_a),
+ *   x[video rows] = embed(z_video; patch_v)                      (h3_embed_rows)
+ *   x = trunk(x)                                                 (h3_trunk_forward)
+ *   z_video += dsigma_video * head_v(x[video rows]),  z_audio += dsigma_audio * head_a(x[audio rows])
+ *                                                                (h3_head_forward)
+ * io: the entry / exit weights (device f32) and segment sizes; table: the blocks' table as for
+ * h3_trunk_forward; table_f: the final table [T][6H] (h3_final_modcache_build); tag, tidx, pos:
+ * this transition's per-row tags, table rows and positions; x: device bf16 [N, H] scratch of
+ * the hidden stream (overwritten).  The latents stay on the device across transitions. */
+typedef struct {
+  int text_rows, cond_rows, audio_rows, video_rows;
+  int k_video, k_audio;                      /* latent features per row: 96 and 32 */
+  const float* patch_v; const float* patch_v_b;  /* [H, k_video], [H] (bias nullable) */
+  const float* patch_a; const float* patch_a_b;  /* [H, k_audio], [H] */
+  const float* head_v; const float* head_v_b;    /* [k_video, H], [k_video] */
+  const float* head_a; const float* head_a_b;    /* [k_audio, H], [k_audio] */
+} h3_io_w;
+
+h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_blocks, const void* table,
+                          const void* table_f, int T, const h3_io_w* io, const void* text_x, const float* z_cond,
+                          float* z_video, float* z_audio, void* x, const uint8_t* tag, const int32_t* tidx,
+                          const float* pos, float dsigma_video, float dsigma_audio, void* workspace, size_t ws_bytes,
+                          unsigned flags, void* stream);
+
 /* ---- step entry points (each row of the block on its own; used for per-step parity) ---- */
 
 /* a1 / a6 -- gather + LayerNorm + modulate ("minimax-h3-mlx" README, "AdaLN: measure, do not

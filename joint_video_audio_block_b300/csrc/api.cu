@@ -435,4 +435,47 @@ h3_status h3_trunk_forward(const h3_dims* dims, const h3_block_w* blocks, int n_
   return H3_OK;
 }
 
+h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_blocks, const void* table,
+                          const void* table_f, int T, const h3_io_w* io, const void* text_x, const float* z_cond,
+                          float* z_video, float* z_audio, void* x, const uint8_t* tag, const int32_t* tidx,
+                          const float* pos, float dsigma_video, float dsigma_audio, void* workspace, size_t ws_bytes,
+                          unsigned flags, void* stream) {
+  if (!dims_ok(dims) || !io || !x || !table_f || !tag || !tidx) return H3_EINVAL;
+  const int H = dims->hidden;
+  const int L = io->text_rows, C = io->cond_rows, A = io->audio_rows, V = io->video_rows;
+  if (L < 0 || C < 0 || A < 0 || V < 0 || (L && !text_x) || (C && !z_cond) || (A && !z_audio) || (V && !z_video))
+    return H3_EINVAL;
+  const int n = L + C + A + V;
+  const size_t row_bytes = static_cast<size_t>(H) * 2;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* xb = static_cast<char*>(x);
+  const long long tf_stride = 6LL * H;
+  h3_status s = H3_OK;
+  // entry
+  if (L && cudaMemcpyAsync(xb, text_x, L * row_bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return H3_ECUDA;
+  if (C && (s = h3_embed_rows(dims, z_cond, io->k_video, io->patch_v, io->patch_v_b, C, xb + L * row_bytes, stream)))
+    return s;
+  if (A && (s = h3_embed_rows(dims, z_audio, io->k_audio, io->patch_a, io->patch_a_b, A,
+                              xb + static_cast<size_t>(L + C) * row_bytes, stream)))
+    return s;
+  if (V && (s = h3_embed_rows(dims, z_video, io->k_video, io->patch_v, io->patch_v_b, V,
+                              xb + static_cast<size_t>(L + C + A) * row_bytes, stream)))
+    return s;
+  // trunk
+  if ((s = h3_trunk_forward(dims, blocks, n_blocks, table, T, x, n, tag, tidx, pos, workspace, ws_bytes, flags,
+                            stream)))
+    return s;
+  // exit + Euler transition
+  if (A && (s = h3_head_forward(dims, xb + static_cast<size_t>(L + C) * row_bytes, A, tag + (L + C), tidx + (L + C),
+                                table_f, tf_stride, io->head_a, io->head_a_b, io->k_audio, nullptr, z_audio,
+                                dsigma_audio, stream)))
+    return s;
+  if (V && (s = h3_head_forward(dims, xb + static_cast<size_t>(L + C + A) * row_bytes, V, tag + (L + C + A),
+                                tidx + (L + C + A), table_f, tf_stride, io->head_v, io->head_v_b, io->k_video,
+                                nullptr, z_video, dsigma_video, stream)))
+    return s;
+  (void)st;
+  return H3_OK;
+}
+
 }  // extern "C"

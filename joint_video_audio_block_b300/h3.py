@@ -25,7 +25,7 @@ EXPORTS = (
     "h3_linear_forward", "h3_qknorm_rope", "h3_qknorm_rope_static", "h3_attention", "h3_last_device_error",
     "h3_status_str", "h3_kernel_timer_start", "h3_kernel_timer_read", "h3_qkv_project",
     "h3_qkv_project_workspace_size", "h3_diag_expire_wait", "h3_attention_sparse", "h3_embed_rows",
-    "h3_final_modcache_build", "h3_head_forward", "h3_sigma_schedule",
+    "h3_final_modcache_build", "h3_head_forward", "h3_sigma_schedule", "h3_denoise_step",
 )
 
 # largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
@@ -52,6 +52,14 @@ class h3_linear(ctypes.Structure):
 class h3_block_w(ctypes.Structure):
     _fields_ = [("qkv", h3_linear), ("o", h3_linear), ("fc1", h3_linear), ("fc2", h3_linear),
                 ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p)]
+
+
+class h3_io_w(ctypes.Structure):
+    _fields_ = [("text_rows", ctypes.c_int), ("cond_rows", ctypes.c_int), ("audio_rows", ctypes.c_int),
+                ("video_rows", ctypes.c_int), ("k_video", ctypes.c_int), ("k_audio", ctypes.c_int),
+                ("patch_v", ctypes.c_void_p), ("patch_v_b", ctypes.c_void_p), ("patch_a", ctypes.c_void_p),
+                ("patch_a_b", ctypes.c_void_p), ("head_v", ctypes.c_void_p), ("head_v_b", ctypes.c_void_p),
+                ("head_a", ctypes.c_void_p), ("head_a_b", ctypes.c_void_p)]
 
 
 _lib = None
@@ -82,6 +90,8 @@ def lib():
             "h3_final_modcache_build": (i32, [D, vp, i32, i32, vp, vp, vp, vp]),
             "h3_head_forward": (i32, [D, vp, i32, vp, vp, vp, i64, vp, vp, i32, vp, vp, ctypes.c_float, vp]),
             "h3_sigma_schedule": (i32, [i32, ctypes.c_float, ctypes.POINTER(ctypes.c_float)]),
+            "h3_denoise_step": (i32, [D, BW, i32, vp, vp, i32, ctypes.POINTER(h3_io_w), vp, vp, vp, vp, vp, vp, vp, vp,
+                                      ctypes.c_float, ctypes.c_float, vp, sz, u32, vp]),
             "h3_last_device_error": (i32, [vp, ctypes.POINTER(u32)]),
             "h3_kernel_timer_start": (i32, [i32]),
             "h3_diag_expire_wait": (i32, [u32, vp]),
@@ -209,6 +219,25 @@ def h3_sigma_schedule(steps: int, shift: float) -> list:
     buf = (ctypes.c_float * (steps + 1))()
     _check(lib().h3_sigma_schedule(steps, shift, buf), "h3_sigma_schedule")
     return [buf[i] for i in range(steps + 1)]
+
+
+def h3_denoise_step(dims, blocks, n_blocks, table, table_f, T, io, text_x, z_cond, z_video, z_audio, x, tag, tidx, pos,
+                    dsigma_video, dsigma_audio, workspace, ws_bytes, flags, stream):
+    arr = (h3_block_w * n_blocks)(*blocks)
+    _check(lib().h3_denoise_step(ctypes.byref(dims), arr, n_blocks, table, table_f, T, ctypes.byref(io), text_x, z_cond,
+                                 z_video, z_audio, x, tag, tidx, pos, dsigma_video, dsigma_audio, workspace, ws_bytes,
+                                 flags, stream), "h3_denoise_step")
+
+
+def make_io_w(t: dict, text_rows, cond_rows, audio_rows, video_rows, k_video=96, k_audio=32):
+    """h3_io_w over device float32 tensors named like synth.io_weights()."""
+    io = h3_io_w()
+    io.text_rows, io.cond_rows, io.audio_rows, io.video_rows = text_rows, cond_rows, audio_rows, video_rows
+    io.k_video, io.k_audio = k_video, k_audio
+    for f in ("patch_v", "patch_v_b", "patch_a", "patch_a_b", "head_v", "head_v_b", "head_a", "head_a_b"):
+        setattr(io, f, ptr(t.get(f)))
+    io._refs = dict(t)
+    return io
 
 
 def h3_last_device_error(stream):

@@ -57,3 +57,26 @@ def workspace(dims: _h3.h3_dims, n_rows: int, device="cuda") -> torch.Tensor:
     if nbytes == 0 and n_rows > 0:
         raise _h3.H3Error(_h3.H3_EINVAL, "h3_workspace_size")
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def sampler_plan(steps: int, video_shift: float = 12.0, audio_shift: float = 3.0):
+    """Host-side plan of a run: the video and audio sampling grids (h3_sigma_schedule), the
+    distinct timesteps (1000 sigma, float32) of the transitions in descending order -- the rows
+    of the modulation tables -- and, per transition, the table row of each schedule."""
+    sv = np.asarray(_h3.h3_sigma_schedule(steps, video_shift), np.float32)
+    sa = np.asarray(_h3.h3_sigma_schedule(steps, audio_shift), np.float32)
+    tv = np.float32(1000.0) * sv[:steps]
+    ta = np.float32(1000.0) * sa[:steps]
+    values = np.array(sorted(set(tv.tolist()) | set(ta.tolist()), reverse=True), np.float32)
+    index = {float(v): i for i, v in enumerate(values)}
+    vidx = [index[float(v)] for v in tv]
+    aidx = [index[float(v)] for v in ta]
+    return values, sv, sa, vidx, aidx
+
+
+def step_tidx(tidx: torch.Tensor, audio_rows: slice, vidx: int, aidx: int) -> torch.Tensor:
+    """Per-row table rows of one transition: the audio rows follow the audio schedule, every
+    other row (text, conditions, video) the video schedule."""
+    tidx.fill_(vidx)
+    tidx[audio_rows] = aidx
+    return tidx

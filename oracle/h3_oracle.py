@@ -453,6 +453,35 @@ def euler_step(z, v, sigma_now: float, sigma_next: float) -> np.ndarray:
     return np.asarray(z, dtype=np.float64) + (float(sigma_next) - float(sigma_now)) * np.asarray(v, dtype=np.float64)
 
 
+def denoise_step(text_x, z_cond, z_audio, z_video, io, block_weight_list, table_bf16, table_f, tag, tidx, pos, dims,
+                 dsigma_video: float, dsigma_audio: float):
+    """One sampler transition over the packed sequence [text | cond | audio | video]
+    (minimax-h3-mlx README, "Architecture" and "Layout"; mlx-h3 README, "Generate": video and
+    audio advance on their own sigma grids): the entry projections write the latent rows into
+    the hidden stream (stored as bf16, as the stream is), the trunk runs, the output heads give
+    each modality's velocity and the Euler step moves its latents.  Returns (z_audio, z_video).
+    io: synth.io_weights() layout; text_x: the projected text rows (bf16 values)."""
+    H = dims.hidden
+    parts = [np.asarray(text_x, dtype=np.float64)]
+    if len(z_cond):
+        parts.append(round_bf16(embed_rows(z_cond, io["patch_v"], io["patch_v_b"])))
+    parts.append(round_bf16(embed_rows(z_audio, io["patch_a"], io["patch_a_b"])))
+    parts.append(round_bf16(embed_rows(z_video, io["patch_v"], io["patch_v_b"])))
+    x = np.concatenate(parts, axis=0)
+    x = trunk_forward(x, block_weight_list, table_bf16, tag, tidx, pos, dims)
+    a0 = len(text_x) + len(z_cond)
+    v0 = a0 + len(z_audio)
+    out = []
+    for r0, z, w, b, ds in ((a0, z_audio, io["head_a"], io["head_a_b"], dsigma_audio),
+                            (v0, z_video, io["head_v"], io["head_v_b"], dsigma_video)):
+        rows = slice(r0, r0 + len(z))
+        shift = final_modulation(table_f, tag[rows], tidx[rows], 0, H)
+        scale = final_modulation(table_f, tag[rows], tidx[rows], 1, H)
+        v = head_forward(x[rows], shift, scale, w, b, dims.ln_eps)
+        out.append(euler_step(z, v, 0.0, ds))
+    return out[0], out[1]
+
+
 # ----------------------------------------------------------------------------------------
 # work model
 # ----------------------------------------------------------------------------------------

@@ -136,3 +136,66 @@ def test_head_forward_and_euler(name, modality):
     z_ref = O.euler_step(z0, ref, 0.0, dsig)
     bound_z = abs(dsig) * bound + 2.0 ** -24 * np.abs(z_ref) * 2
     assert np.all(np.abs(z.cpu().numpy() - z_ref) <= bound_z)
+
+
+def test_denoise_steps_tiny():
+    """Three sampler transitions of a 2-block tiny model end to end through h3_denoise_step
+    against the oracle's composition (entry -> trunk -> heads -> Euler), with the run's own
+    video (shift 12) and audio (shift 3) grids and per-row table rows per transition."""
+    cfg = synth.CONFIGS["tiny"]
+    d = cfg.dims
+    H, n, B, S = d.hidden, cfg.layout.n_rows, 2, 3
+    dims = R.dims_of(d)
+    lay = cfg.layout
+    L, C, A, V = lay.text, lay.n_cond, lay.audio, lay.n_video
+    values, sv, sa, vidx, aidx = R.sampler_plan(S)
+    # tables for the run's distinct timesteps (oracle-built bf16 values feed both sides)
+    temb = synth.sinusoidal_temb(values, d.temb_dim)
+    blocks = [synth.block_weights(cfg, b) for b in range(B)]
+    aw = [synth.adaln_weights(cfg, b) for b in range(B)]
+    _, tbf = O.modcache(temb, [a for a, _ in aw], [b for _, b in aw])
+    io = synth.io_weights(cfg)
+    _, tf = O.modcache(temb, [io["final_w"]], [io["final_b"]])
+    tf = tf[:, 0, :]
+    tag, _, pos = synth.packed_rows(cfg)
+    text_bits = synth.activations(cfg)[:L]
+    zv0, za0 = synth.latents(cfg)
+    z_cond, z_video = zv0[:C], zv0[C:]
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    # device state
+    wts = [R.upload_block(w) for w in blocks]
+    bws = [h3.make_block_w(w) for w in wts]
+    io_d = {k: dev(v) for k, v in io.items() if k.startswith(("patch", "head"))}
+    iow = h3.make_io_w(io_d, L, C, A, V)
+    table = R.bf16_from_bits(O.to_bf16_bits(tbf))
+    table_f = R.bf16_from_bits(O.to_bf16_bits(tf))
+    text_x = R.bf16_from_bits(text_bits)
+    zc_d, zv_d, za_d = dev(z_cond), dev(z_video), dev(za0)
+    x = torch.empty(n, H, dtype=torch.bfloat16, device="cuda")
+    tag_d, pos_d = dev(tag), dev(pos)
+    tidx_d = torch.empty(n, dtype=torch.int32, device="cuda")
+    ws = R.workspace(dims, n)
+    T = len(values)
+    # oracle state
+    zv_ref, za_ref = z_video.astype(np.float64), za0.astype(np.float64)
+    audio = slice(L + C, L + C + A)
+    for i in range(S):
+        R.step_tidx(tidx_d, audio, vidx[i], aidx[i])
+        dsv, dsa = float(sv[i + 1] - sv[i]), float(sa[i + 1] - sa[i])
+        h3.h3_denoise_step(dims, bws, B, table.data_ptr(), table_f.data_ptr(), T, iow, text_x.data_ptr(),
+                           zc_d.data_ptr() if C else None, zv_d.data_ptr(), za_d.data_ptr(), x.data_ptr(),
+                           tag_d.data_ptr(), tidx_d.data_ptr(), pos_d.data_ptr(), dsv, dsa, ws.data_ptr(), ws.numel(),
+                           0, h3.stream_ptr())
+        tidx = np.full(n, vidx[i], np.int32)
+        tidx[audio] = aidx[i]
+        za_ref, zv_ref = O.denoise_step(O.widen_bf16(text_bits), z_cond, za_ref, zv_ref, io, blocks, tbf, tf, tag, tidx,
+                                        pos, d, dsv, dsa)
+    _sync()
+    # compare the distance the latents travelled (z itself is dominated by the initial noise)
+    for got, ref, z0, what in ((zv_d, zv_ref, z_video, "video"), (za_d, za_ref, za0, "audio")):
+        g = got.cpu().numpy().astype(np.float64) - z0
+        r = ref - z0
+        rel = np.linalg.norm(g - r) / np.linalg.norm(r)
+        mx = np.abs(g - r).max() / np.abs(r).max()
+        print(f"denoise {what}: moved rms {np.sqrt(np.mean(r * r)):.3e}; rel_l2={rel:.3e} max_abs/max|ref|={mx:.3e}")
+        assert rel <= 1e-2 and mx <= 5e-2
