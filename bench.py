@@ -319,6 +319,38 @@ def run_ours(args, cfg, rank, world, local_rank):
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
     e2e_value = whole_job_rate(world, N, args.steps, e2e_s)
 
+    # one whole sampler transition at the same workload: entry projections, the trunk, the
+    # output heads and the Euler update of the float32 latents (h3_denoise_step)
+    lay = cfg.layout
+    L, C, A, V = lay.text, lay.n_cond, lay.audio, lay.n_video
+    g = torch.Generator(device=dev)
+    g.manual_seed(cfg.seed + 77)
+    rnd = lambda *shape, std=1.0: torch.randn(*shape, generator=g, device=dev) * std  # noqa: E731
+    kv, ka = synth.VIDEO_FEATURES, synth.AUDIO_FEATURES
+    io_d = {"patch_v": rnd(d.hidden, kv, std=0.02), "patch_v_b": rnd(d.hidden, std=0.02),
+            "patch_a": rnd(d.hidden, ka, std=0.02), "patch_a_b": rnd(d.hidden, std=0.02),
+            "head_v": rnd(kv, d.hidden, std=0.02), "head_v_b": rnd(kv, std=0.02),
+            "head_a": rnd(ka, d.hidden, std=0.02), "head_a_b": rnd(ka, std=0.02)}
+    iow = h3.make_io_w(io_d, L, C, A, V, kv, ka)
+    table_f = (rnd(T, 6 * d.hidden, std=0.5)).to(torch.bfloat16)
+    text_x = x0[:L].clone()
+    zc, zv, za = rnd(C, kv), rnd(V, kv), rnd(A, ka)
+
+    def transition():
+        h3.h3_denoise_step(dims, bws, B, table.data_ptr(), table_f.data_ptr(), T, iow, text_x.data_ptr(),
+                           zc.data_ptr() if C else None, zv.data_ptr(), za.data_ptr(), x.data_ptr(), tag_d.data_ptr(),
+                           tidx_d.data_ptr(), pos_d.data_ptr(), -0.01, -0.01, ws.data_ptr(), ws.numel(), 0, sp)
+
+    transition()
+    torch.cuda.synchronize()
+    tc, td = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tc.record()
+    for _ in range(2):
+        transition()
+    td.record()
+    torch.cuda.synchronize()
+    transition_ms = tc.elapsed_time(td) / 2
+
     hbm_peak, bf16_peak, bf16_sus, peak_kind = _peaks()
     lin_f, att_f = _flops(cfg, N)
     att_ms = statistics.mean(att_durations) if att_durations else float("nan")
@@ -350,7 +382,9 @@ def run_ours(args, cfg, rank, world, local_rank):
             "modcache": {"ms": modcache_ms, "timesteps": T, "blocks": B,
                          "GB_per_s": modcache_bytes / (modcache_ms / 1e3) / 1e9},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * (1 + 8 * B),  # rope table + 8 kernels per block
+            "sampler_transition": {"ms": transition_ms, "tokens_per_s": N / (transition_ms / 1e3),
+                                   "what": "entry projections + trunk + output heads + Euler (h3_denoise_step)"},
+            "gpu_launches": args.steps * (1 + 7 * B),  # rope table + 7 kernels per block
             "clocks": clk,
             "cpu_baseline": cpu,
         }

@@ -8,6 +8,8 @@
 //
 // Outputs are laid out for the attention kernel: q and k head-major [nh][N][hd] (K-major
 // operands of S = Q K^T) and v transposed per head [nh][hd][ld_vt] (K-major operand of O = P V).
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace h3 {
@@ -59,41 +61,78 @@ __global__ void __launch_bounds__(256) qknorm_rope_kernel(const bf16* __restrict
   const bool first_half = lane < PART;
   const size_t row_stride = static_cast<size_t>(3) * nh * HD;
 
-  for (int rr = warp; rr < 64; rr += 8) {
-    const int r = r0 + rr;
-    if (r >= n_rows) {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) sv[rr][lane * EPL + e] = f2bf(0.f);
-      continue;
+  // EPL consecutive bf16 per lane move as one 4- or 8-byte word; two rows per iteration keep
+  // twice the loads in flight
+  using Vec = typename std::conditional<EPL == 4, uint2, uint32_t>::type;
+  auto unpack = [](const Vec& u, float* f) {
+    if constexpr (EPL == 4) {
+      f[0] = bf16lo(u.x);
+      f[1] = bf16hi(u.x);
+      f[2] = bf16lo(u.y);
+      f[3] = bf16hi(u.y);
+    } else {
+      f[0] = bf16lo(u);
+      f[1] = bf16hi(u);
     }
-    const bf16* base = qkv + static_cast<size_t>(r) * row_stride + static_cast<size_t>(h) * 3 * HD;
+  };
+  auto pack = [](const float* f) -> Vec {
+    if constexpr (EPL == 4) {
+      return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+    } else {
+      return pack_bf16x2(f[0], f[1]);
+    }
+  };
+#pragma unroll 1
+  for (int rb = warp; rb < 64; rb += 16) {
+    Vec in[2][3];
+    float2 cr[2][EPL];
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      float a[EPL];
+    for (int u = 0; u < 2; ++u) {
+      const int r = r0 + rb + 8 * u;
+      if (r < n_rows) {
+        const bf16* base = qkv + static_cast<size_t>(r) * row_stride + static_cast<size_t>(h) * 3 * HD + lane * EPL;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) a[e] = bf2f(base[which * HD + lane * EPL + e]);
-      if (has_norm) {
-        float ss = 0.f;
+        for (int which = 0; which < 3; ++which) in[u][which] = *reinterpret_cast<const Vec*>(base + which * HD);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) ss += a[e] * a[e];
-        ss = warp_sum(ss);
-        const float rinv = rsqrtf(ss / HD + eps);
+        for (int e = 0; e < EPL; ++e) cr[u][e] = cs[static_cast<size_t>(r) * HALF + pi + e];
+      } else {
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) a[e] = a[e] * rinv * (which ? wk[e] : wq[e]);
-      }
-      bf16* dst = (which ? k : q) + (static_cast<size_t>(h) * n_rows + r) * HD + lane * EPL;
+        for (int which = 0; which < 3; ++which) in[u][which] = Vec{};
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        const float b = __shfl_xor_sync(0xffffffffu, a[e], PART);
-        const float2 c = cs[static_cast<size_t>(r) * HALF + pi + e];
-        // first half holds x_i, partner x_{i+hd/2}: x_i cos - x_{i+hd/2} sin
-        // second half holds x_{i+hd/2}, partner x_i: x_i sin + x_{i+hd/2} cos
-        const float out = first_half ? (a[e] * c.x - b * c.y) : (b * c.y + a[e] * c.x);
-        dst[e] = f2bf(out);
+        for (int e = 0; e < EPL; ++e) cr[u][e] = make_float2(1.f, 0.f);
       }
     }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) sv[rr][lane * EPL + e] = base[2 * HD + lane * EPL + e];
+    for (int u = 0; u < 2; ++u) {
+      const int rr = rb + 8 * u;
+      const int r = r0 + rr;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        float a[EPL];
+        unpack(in[u][which], a);
+        if (has_norm) {
+          float ss = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) ss += a[e] * a[e];
+          ss = warp_sum(ss);
+          const float rinv = rsqrtf(ss / HD + eps);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) a[e] = a[e] * rinv * (which ? wk[e] : wq[e]);
+        }
+        float out[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float b = __shfl_xor_sync(0xffffffffu, a[e], PART);
+          const float2 c = cr[u][e];
+          // first half holds x_i, partner x_{i+hd/2}: x_i cos - x_{i+hd/2} sin
+          // second half holds x_{i+hd/2}, partner x_i: x_i sin + x_{i+hd/2} cos
+          out[e] = first_half ? (a[e] * c.x - b * c.y) : (b * c.y + a[e] * c.x);
+        }
+        if (r < n_rows)
+          *reinterpret_cast<Vec*>((which ? k : q) + (static_cast<size_t>(h) * n_rows + r) * HD + lane * EPL) = pack(out);
+      }
+      *reinterpret_cast<Vec*>(&sv[rr][lane * EPL]) = in[u][2];  // zeros for rows past the end
+    }
   }
   __syncthreads();
   // transposed store of v: 16-byte chunks of 8 consecutive rows for one d
