@@ -104,3 +104,37 @@ def test_sigma_schedule_is_the_oracle_grid(h3mod):
     for steps, shift in ((40, 12.0), (40, 3.0), (8, 12.0), (77, 1.0), (1, 3.0)):
         got = np.asarray(h3mod.h3_sigma_schedule(steps, shift), np.float32)
         np.testing.assert_array_equal(got, O.shifted_sigmas(steps, shift))
+
+
+def test_more_invalid_arguments_rejected_before_launch(h3mod):
+    """Misalignment and range errors of the newer entry points are refused on the host."""
+    L = h3mod.lib()
+    d = _tiny_dims(h3mod)
+    odd = 0x1000 + 2  # not 16-byte aligned (never dereferenced: the call must refuse first)
+    al = 0x2000
+    # attention: misaligned q; sparse attention: no mask
+    assert L.h3_attention(ctypes.byref(d), odd, al, al, 72, al, 72, 0, None) == h3mod.H3_EINVAL
+    assert L.h3_attention_sparse(ctypes.byref(d), al, al, al, 72, al, 72, None, None) == h3mod.H3_EINVAL
+    # ld_vt must cover the rows and be a multiple of 8
+    assert L.h3_attention(ctypes.byref(d), al, al, al, 70, al, 72, 0, None) == h3mod.H3_EINVAL
+    # entry / exit: bad widths, both outputs missing, misaligned rows
+    assert L.h3_embed_rows(ctypes.byref(d), al, 0, al, None, 8, al, None) == h3mod.H3_EINVAL
+    assert L.h3_embed_rows(ctypes.byref(d), al, 96, al, None, 8, odd, None) == h3mod.H3_EINVAL
+    assert L.h3_head_forward(ctypes.byref(d), al, 8, al, al, al, 6 * 192, al, None, 96, None, None,
+                             ctypes.c_float(0.0), None) == h3mod.H3_EINVAL
+    assert L.h3_head_forward(ctypes.byref(d), al, 8, al, al, al, 6 * 192, al, None, 129, al, None,
+                             ctypes.c_float(0.0), None) == h3mod.H3_EINVAL
+    assert L.h3_head_forward(ctypes.byref(d), al, 8, al, al, al, 5 * 192, al, None, 96, al, None,
+                             ctypes.c_float(0.0), None) == h3mod.H3_EINVAL
+    # sampler grid: no steps / non-positive shift
+    buf = (ctypes.c_float * 4)()
+    assert L.h3_sigma_schedule(0, ctypes.c_float(3.0), buf) == h3mod.H3_EINVAL
+    assert L.h3_sigma_schedule(3, ctypes.c_float(0.0), buf) == h3mod.H3_EINVAL
+    # the static-scratch variant refuses sizes beyond its array, and the diagnostic its range
+    n = h3mod.H3_QKROPE_STATIC_MAX_PAIRS // 32 + 1  # head_dim 64 -> 32 pairs per row
+    assert L.h3_qknorm_rope_static(ctypes.byref(d), al, al, None, None, al, al, al, (n + 63) // 64 * 64, n,
+                                   None) == h3mod.H3_EINVAL
+    assert L.h3_diag_expire_wait(0, None) == h3mod.H3_EINVAL
+    assert L.h3_diag_expire_wait(2_000_000, None) == h3mod.H3_EINVAL
+    # the timer: negative capacity
+    assert L.h3_kernel_timer_start(-1) == h3mod.H3_EINVAL
