@@ -99,10 +99,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, bus_id, rank):
+    def __init__(self, bus_id, rank, path=None):
+        import tempfile
+
         self.bus = bus_id
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(), f"h3_bench_clocks_rank{rank}.csv")
 
     def start(self):
         try:
@@ -268,7 +270,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
     except Exception:
         bus = None
-    clocks = ClockSampler(bus, rank)
+    clocks = ClockSampler(bus, rank, args.clocks_csv.replace("{rank}", str(rank)) if args.clocks_csv else None)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -402,6 +404,7 @@ def main():
     ap.add_argument("--workload", default="trunk33720")
     ap.add_argument("--blocks", type=int, default=0, help="override the block count (diagnostics only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None, help="where to keep the raw clock samples ({rank} is replaced)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
