@@ -3,7 +3,8 @@
  *
  * C ABI.  Every pointer argument named "device" is a CUDA device pointer owned by the caller;
  * pointers named "host" are host memory.  The library allocates no device memory: scratch
- * space comes from the caller's workspace.  All compute calls are asynchronous on `stream`
+ * space comes from the caller's workspace (the one exception, h3_qknorm_rope_static, uses a
+ * fixed array that is part of the loaded library).  All compute calls are asynchronous on `stream`
  * (a cudaStream_t passed as void*; NULL = the legacy default stream) and return before the
  * GPU work finishes.  Tensors are dense and row-major unless a stride is given; "bf16" means
  * IEEE bfloat16 bit patterns (2 bytes), "f32" float32.
