@@ -134,6 +134,9 @@ class Dims:
 
 TINY = Dims(hidden=192, heads=4, head_dim=64, ffn=512, temb_dim=96)
 H3 = Dims(hidden=5376, heads=56, head_dim=128, ffn=14336, temb_dim=2688)
+# the H3 head geometry (128-wide heads, same rotary split) at a fifth of the width: a 50-block
+# trunk of it is small enough for the fp64 oracle to run in well under a minute
+NARROW = Dims(hidden=1024, heads=8, head_dim=128, ffn=2816, temb_dim=256)
 
 
 @dataclass(frozen=True)
@@ -200,6 +203,10 @@ CONFIGS = {
     "block1829": Config("block1829", H3, Layout(256, (), 37, (6, 16, 16)), seed=1),
     "block12936": Config("block12936", H3, Layout(256, (), 200, (32, 15, 26)), seed=2),
     "block12936_int8": Config("block12936_int8", H3, Layout(256, (), 200, (32, 15, 26)), seed=3, int8=True),
+    "trunk50x1829_narrow": Config(
+        "trunk50x1829_narrow", NARROW, Layout(256, (), 37, (6, 16, 16)), seed=5, n_blocks=50, n_timesteps=77,
+        timesteps=_T77,
+    ),
     "trunk33720": Config(
         "trunk33720", H3, Layout(256, (24, 42), 200, (32, 24, 42)), seed=4, n_blocks=50, n_timesteps=77,
         timesteps=_T77,

@@ -1,0 +1,104 @@
+"""GPU parity at full depth: a 50-block trunk through h3_trunk_forward against the oracle.
+
+The trunk repeats the block 50 times ("minimax-h3-mlx" README, "Architecture"), so rounding
+that is harmless in one block could grow along the residual stream.  This test runs all 50
+blocks at 1,829 packed rows with per-row tags and the two timestep indices of a sampling
+step, on the H3 head geometry (128-wide heads, the same rotary split) at a narrower width
+(hidden 1024, 8 heads, SwiGLU 2816): the full-width 50-block oracle takes about ten minutes
+of fp64 on a 16-core host, this one a minute or two.  The kernels, tiles and epilogues it
+exercises are the ones the full-width trunk uses; only the loop trip counts differ.
+
+Bars.  The tolerance stated for a block output (relative L2 <= 1e-2, max-abs <= 5e-2 of
+max|ref|) is checked for every one of the 50 blocks, each against the oracle's block applied
+to the same (GPU-produced) input.  For the whole trunk the reference is the exact oracle and
+the bar is the bf16 floor: the GPU's accumulated error may be at most twice that of the oracle
+run with bf16 storage at the GPU's rounding points.  (At this depth bf16 storage at those
+points, with exact arithmetic everywhere else, already moves the output by about 1.7% in
+relative L2, so the per-block bound does not carry over to 50 blocks.)
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import oracle.h3_oracle as O  # noqa: E402
+import synth  # noqa: E402
+from joint_video_audio_block_b300 import h3, runtime as R  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _err(gpu, ref):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rel = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300)
+    mx = float(np.abs(gpu - ref).max()) / max(float(np.abs(ref).max()), 1e-300)
+    return rel, mx
+
+
+def test_trunk_50_blocks_narrow():
+    cfg = synth.CONFIGS["trunk50x1829_narrow"]
+    d, n, B = cfg.dims, cfg.layout.n_rows, cfg.n_blocks
+    dims = R.dims_of(d)
+    x_bits = synth.activations(cfg)
+    tag, tidx, pos = synth.packed_rows(cfg, step=3)
+    assert len(set(tidx.tolist())) == 2  # video and audio rows at different timesteps
+    aw = [synth.adaln_weights(cfg, b) for b in range(B)]
+    _, table_bf = O.modcache(synth.temb(cfg), [a for a, _ in aw], [b for _, b in aw])
+    T = table_bf.shape[0]
+    w_bits = [synth.block_weights(cfg, b) for b in range(B)]
+
+    wts = [R.upload_block(w) for w in w_bits]
+    bws = [h3.make_block_w(w) for w in wts]
+    x0 = R.bf16_from_bits(x_bits)
+    table = R.bf16_from_bits(O.to_bf16_bits(table_bf))
+    tag_d = torch.from_numpy(tag).cuda()
+    tidx_d = torch.from_numpy(tidx).cuda()
+    pos_d = torch.from_numpy(pos).cuda()
+    ws = R.workspace(dims, n)
+    H = d.hidden
+
+    def device_ok():
+        torch.cuda.synchronize()
+        dev, site = h3.h3_last_device_error(h3.stream_ptr())
+        assert dev == h3.H3_OK, f"device error word set: site {site:#x}"
+
+    # the whole trunk in one call
+    x = x0.clone()
+    h3.h3_trunk_forward(dims, bws, B, table.data_ptr(), T, x.data_ptr(), n, tag_d.data_ptr(), tidx_d.data_ptr(),
+                        pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0, h3.stream_ptr())
+    device_ok()
+    got = R.f32_from_bf16(x)
+    assert np.isfinite(got).all()
+
+    # block by block: every block output against the oracle's block on the same input
+    xs = x0.clone()
+    worst = (0.0, 0.0, -1)
+    for b in range(B):
+        x_in_bits = O.to_bf16_bits(R.f32_from_bf16(xs))
+        out = torch.empty_like(xs)
+        h3.h3_block_forward(dims, bws[b], table.data_ptr() + b * 18 * H * 2, B * 18 * H, T, xs.data_ptr(),
+                            out.data_ptr(), n, tag_d.data_ptr(), tidx_d.data_ptr(), pos_d.data_ptr(), ws.data_ptr(),
+                            ws.numel(), 0, h3.stream_ptr())
+        device_ok()
+        ref_b = O.block_forward(x_in_bits, w_bits[b], table_bf[:, b, :], tag, tidx, pos, d)
+        r_b, m_b = _err(R.f32_from_bf16(out), ref_b)
+        assert r_b <= 1e-2 and m_b <= 5e-2, f"block {b}: rel_l2={r_b:.3e} max_abs/max|ref|={m_b:.3e}"
+        worst = max(worst, (r_b, m_b, b))
+        xs = out
+    print(f"per-block worst: rel_l2={worst[0]:.3e} max_abs/max|ref|={worst[1]:.3e} (block {worst[2]})")
+    assert torch.equal(xs, x)  # the trunk call is exactly the 50 block calls
+
+    # the accumulated error at the bf16 floor
+    ref = O.trunk_forward(x_bits, w_bits, table_bf, tag, tidx, pos, d)
+    ref_e = O.trunk_forward(x_bits, w_bits, table_bf, tag, tidx, pos, d, emulate_bf16=True)
+    r, m = _err(got, ref)
+    r_e, m_e = _err(ref_e, ref)
+    r_ge, _ = _err(got, ref_e)
+    print(f"trunk 50x1829 narrow: GPU vs exact rel_l2={r:.3e} max_abs/max|ref|={m:.3e}; "
+          f"bf16-storage oracle vs exact rel_l2={r_e:.3e} max_abs/max|ref|={m_e:.3e}; "
+          f"GPU vs bf16-storage oracle rel_l2={r_ge:.3e}; max|ref|={np.abs(ref).max():.3g}")
+    assert r <= 2 * r_e and m <= 2 * m_e
