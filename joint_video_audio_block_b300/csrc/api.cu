@@ -3,8 +3,9 @@
 // The block follows "minimax-h3-mlx" README, "Architecture" / "AdaLN: measure, do not
 // reason" / "Validation":
 //   xn = LN(x)(1 + scale_msa) + shift_msa            adaln_modulate
-//   qkv = xn Wqkv^T + b                               tcgen05 GEMM, bias epilogue
-//   q, k = RoPE(RMSNorm(.)), v^T                      qknorm_rope
+//   qkv = xn Wqkv^T + b                               tcgen05 GEMM
+//   q, k = RoPE(RMSNorm(.)), v^T                      in that GEMM's epilogue (head_dim 128), else
+//                                                     a bias epilogue + qknorm_rope
 //   o = softmax(q k^T / sqrt(hd)) v                   tcgen05 attention
 //   x' = x + gate_msa (o Wo^T + bo)                   tcgen05 GEMM, gate+residual epilogue
 //   xn = LN(x')(1 + scale_mlp) + shift_mlp            adaln_modulate
@@ -474,7 +475,6 @@ h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_b
                                 tidx + (L + C + A), table_f, tf_stride, io->head_v, io->head_v_b, io->k_video,
                                 nullptr, z_video, dsigma_video, stream)))
     return s;
-  (void)st;
   return H3_OK;
 }
 

@@ -46,15 +46,21 @@ extern "C" h3_status h3_kernel_timer_start(int capacity) {
   destroy_events();
   if (capacity == 0) return H3_OK;
   if (cudaGetDevice(&g_timer.device) != cudaSuccess) return H3_ECUDA;
-  g_timer.start.resize(capacity);
-  g_timer.stop.resize(capacity);
+  g_timer.start.reserve(capacity);
+  g_timer.stop.reserve(capacity);
   for (int i = 0; i < capacity; ++i) {
-    if (cudaEventCreate(&g_timer.start[i]) != cudaSuccess || cudaEventCreate(&g_timer.stop[i]) != cudaSuccess) {
-      g_timer.start.resize(i);
-      g_timer.stop.resize(i);
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaEventCreate(&a) != cudaSuccess) {
       destroy_events();
       return H3_ECUDA;
     }
+    if (cudaEventCreate(&b) != cudaSuccess) {
+      cudaEventDestroy(a);
+      destroy_events();
+      return H3_ECUDA;
+    }
+    g_timer.start.push_back(a);
+    g_timer.stop.push_back(b);
   }
   return H3_OK;
 }
