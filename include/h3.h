@@ -51,7 +51,8 @@ typedef enum { H3_W_BF16 = 0, H3_W_INT8_G32 = 1 } h3_wfmt;
 
 /* Block geometry.  hidden H, heads nh, head_dim hd (64 or 128), ffn F, n_tags modality tags.
  * rope_sections: frequency pairs given to the (t, h, w) position axes, summing to hd/2.
- * Requirements: H % 64 == 0, (nh*hd) % 64 == 0, F % 128 == 0. */
+ * Requirements: H % 64 == 0 and H <= 8192, (nh*hd) % 64 == 0, F % 128 == 0, 1 <= n_tags <= 255,
+ * rope_theta > 0, ln_eps >= 0, qk_eps >= 0. */
 typedef struct {
   int hidden, heads, head_dim, ffn, n_tags;
   int rope_sections[3];
