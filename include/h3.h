@@ -287,6 +287,22 @@ h3_status h3_kernel_timer_read(float* ms, int capacity, int* n_recorded);
  * involved.  timeout_us outside the range returns H3_EINVAL. */
 h3_status h3_diag_expire_wait(unsigned timeout_us, void* stream);
 
+/* Diagnostic of the tensor pipe as one issuing thread feeds it (no counterpart on the pages:
+ * it measures the hardware property the attention and GEMM pipelines are designed around).
+ * Launches `ctas` CTAs (1 .. H3_DIAG_MAX_CTAS; one per SM fits), each issuing `batches`
+ * (1 .. 100,000) batches of 16 bf16 MMAs of 128x128x16 (8 with both operands in shared memory,
+ * 8 with A in tensor memory) on whatever the memories hold; nothing is read back.
+ * mode 0: back to back; 1: between the shared-memory-operand and the tensor-memory-operand
+ * MMAs of each batch the issuing thread polls an mbarrier whose phase is already complete and
+ * uses the answer at once; 2: the same poll as a non-blocking test read after the batch;
+ * 3: the blocking poll after the batch instead (mode outside 0..3: H3_EINVAL).
+ * Synchronises `stream` and writes to the host
+ * double *cycles_per_mma the median over CTAs of SM cycles per MMA (64 at full rate).  The
+ * per-CTA counts live in a fixed array inside the library (no allocation).  A wait that runs
+ * out is reported by h3_last_device_error (site 0x302). */
+#define H3_DIAG_MAX_CTAS 1024
+h3_status h3_diag_issue_rate(int mode, int batches, int ctas, double* cycles_per_mma, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device error word.  Returns H3_OK, or
  * H3_ETIMEOUT when a bounded device wait ran out since the last call (*site, if not NULL,
  * receives the site code), or H3_ECUDA if the stream reports a CUDA error. */

@@ -674,6 +674,16 @@ def test_bounded_wait_expires_and_context_survives():
     check_step(R.f32_from_bf16(o), ref, what="attention after an expired wait", spread=1e-3, extra=p_err)
 
 
+def test_issue_rate_diagnostic_issues_its_mmas():
+    """h3_diag_issue_rate really runs its MMAs: no mode can beat the tensor pipe's full rate of
+    64 cycles per 128x128x16 MMA, every CTA finishes, and the error word stays clear."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for mode in range(4):
+        c = h3.h3_diag_issue_rate(mode, 100, sms, h3.stream_ptr())
+        assert 60.0 <= c < 1000.0, (mode, c)
+    sync_ok()
+
+
 def test_zero_rows_and_bad_arguments():
     c = Case("tiny")
     wt = R.upload_block(c.w_bits[0])
