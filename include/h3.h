@@ -295,7 +295,8 @@ h3_status h3_diag_expire_wait(unsigned timeout_us, void* stream);
  * mode 0: back to back; 1: between the shared-memory-operand and the tensor-memory-operand
  * MMAs of each batch the issuing thread polls an mbarrier whose phase is already complete and
  * uses the answer at once; 2: the same poll as a non-blocking test read after the batch;
- * 3: the blocking poll after the batch instead (mode outside 0..3: H3_EINVAL).
+ * 3: the blocking poll after the batch instead; 4: mode 0 while eight more warps, two per SM
+ * sub-partition, run dependent FMA / exp2 arithmetic (mode outside 0..4: H3_EINVAL).
  * Synchronises `stream` and writes to the host
  * double *cycles_per_mma the median over CTAs of SM cycles per MMA (64 at full rate).  The
  * per-CTA counts live in a fixed array inside the library (no allocation).  A wait that runs

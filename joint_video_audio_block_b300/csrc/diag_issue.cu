@@ -14,6 +14,9 @@
 //   mode 2  the same poll at the same point as a non-blocking test whose answer is read only
 //           after the tensor-memory-operand MMAs
 //   mode 3  the blocking poll of mode 1 placed after the tensor-memory-operand MMAs instead
+//   mode 4  mode 0 while eight more warps (two on every SM sub-partition, the issuer's
+//           included, as the attention kernel's softmax warps are) run a dependent chain of
+//           FMA and SFU exp2 until the MMAs are done
 // A full-rate pipe takes 64 cycles per MMA (8,192 FLOP per cycle per SM).
 #include <algorithm>
 #include <vector>
@@ -27,6 +30,7 @@ constexpr unsigned kErrDiagIssue = 0x302;
 constexpr int kIssueSmem = 120 * 1024;
 
 __device__ unsigned long long g_issue_cycles[H3_DIAG_MAX_CTAS];
+__device__ float g_issue_sink;  // keeps the busy warps' arithmetic alive
 
 __device__ __forceinline__ void mma_ts_diag(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -51,15 +55,17 @@ __device__ __forceinline__ uint32_t mbar_test_diag(uint32_t bar, uint32_t parity
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(128, 1) issue_rate_kernel(int batches, unsigned* err) {
+__global__ void __launch_bounds__(384, 1) issue_rate_kernel(int batches, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t s = smem_u32(smem);  // operands: A atoms at s, s + 16K; B atoms at s + 32K, s + 48K
   const uint32_t bar = s + 65536;     // [0] completion of the MMAs; [1] a barrier polled in modes 1, 2
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + 65536 + 64);
+  volatile uint32_t* done = reinterpret_cast<volatile uint32_t*>(smem + 65536 + 128);
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     mbar_init(bar + 8, 1);
+    *done = 0;
     fence_barrier_init();
   }
   if (threadIdx.x < 32) {
@@ -98,6 +104,19 @@ __global__ void __launch_bounds__(128, 1) issue_rate_kernel(int batches, unsigne
     umma_commit(bar);
     mbar_wait(bar, 0, err, kErrDiagIssue);
     g_issue_cycles[blockIdx.x] = clock64() - t0;
+    *done = 1;
+  }
+  if (MODE == 4 && threadIdx.x >= 128) {
+    float a = 1.0f + 1e-3f * threadIdx.x;
+    for (int it = 0; it < (1 << 22) && *done == 0u; ++it) {
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        float e;
+        asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a * -1e-3f));
+        a = fmaf(a, 0.999f, e);
+      }
+    }
+    if (a == -1.0f) g_issue_sink = a;
   }
   tc_fence_before();
   __syncthreads();
@@ -116,7 +135,7 @@ static cudaError_t launch_issue_rate(int batches, int ctas, unsigned* err, cudaS
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  issue_rate_kernel<MODE><<<ctas, 128, kIssueSmem, st>>>(batches, err);
+  issue_rate_kernel<MODE><<<ctas, MODE == 4 ? 384 : 128, kIssueSmem, st>>>(batches, err);
   return cudaGetLastError();
 }
 
@@ -125,7 +144,7 @@ static cudaError_t launch_issue_rate(int batches, int ctas, unsigned* err, cudaS
 using namespace h3;
 
 extern "C" h3_status h3_diag_issue_rate(int mode, int batches, int ctas, double* cycles_per_mma, void* stream) {
-  if (mode < 0 || mode > 3 || batches < 1 || batches > 100000 || ctas < 1 || ctas > H3_DIAG_MAX_CTAS ||
+  if (mode < 0 || mode > 4 || batches < 1 || batches > 100000 || ctas < 1 || ctas > H3_DIAG_MAX_CTAS ||
       !cycles_per_mma)
     return H3_EINVAL;
   unsigned* err = h3_error_word_ptr();
@@ -134,7 +153,8 @@ extern "C" h3_status h3_diag_issue_rate(int mode, int batches, int ctas, double*
   cudaError_t e = mode == 0   ? launch_issue_rate<0>(batches, ctas, err, st)
                   : mode == 1 ? launch_issue_rate<1>(batches, ctas, err, st)
                   : mode == 2 ? launch_issue_rate<2>(batches, ctas, err, st)
-                              : launch_issue_rate<3>(batches, ctas, err, st);
+                  : mode == 3 ? launch_issue_rate<3>(batches, ctas, err, st)
+                              : launch_issue_rate<4>(batches, ctas, err, st);
   if (e != cudaSuccess) return H3_ECUDA;
   std::vector<unsigned long long> cyc(ctas);
   if (cudaMemcpyFromSymbolAsync(cyc.data(), g_issue_cycles, sizeof(unsigned long long) * ctas, 0,

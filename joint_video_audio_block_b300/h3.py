@@ -201,8 +201,8 @@ def h3_diag_expire_wait(timeout_us: int, stream):
 def h3_diag_issue_rate(mode: int, batches: int, ctas: int, stream) -> float:
     """SM cycles per 128x128x16 MMA as one thread issues them: mode 0 back to back, 1 with a
     barrier poll between the 8 shared-memory-operand and 8 tensor-memory-operand MMAs of each
-    batch, 2 with that poll as a test read after the batch, 3 with the poll after the batch;
-    synchronises the stream."""
+    batch, 2 with that poll as a test read after the batch, 3 with the poll after the batch, 4
+    back to back beside eight warps of FMA / exp2 arithmetic; synchronises the stream."""
     out = ctypes.c_double(0.0)
     _check(lib().h3_diag_issue_rate(mode, batches, ctas, ctypes.byref(out), stream), "h3_diag_issue_rate")
     return out.value

@@ -244,13 +244,15 @@ def issue_rate(reps: int):
     """The tensor pipe fed by one issuing thread (h3_diag_issue_rate), one CTA per SM, 2,000
     batches of 16 MMAs of 128x128x16 per CTA (8 with shared-memory operands, then 8 with A in
     tensor memory): back to back, with a barrier poll between the two halves, with that poll as
-    a test read after the batch, and with the poll after the batch.  Prints one line per mode
+    a test read after the batch, with the poll after the batch, and back to back while eight more
+    warps run arithmetic beside the issuer.  Prints one line per mode
     with the median cycles per MMA over `reps` launches (64 = full rate)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     names = ("back to back", "blocking poll after the shared-memory-operand MMAs",
-             "test there, answer read after the batch", "blocking poll after the tensor-memory-operand MMAs")
+             "test there, answer read after the batch", "blocking poll after the tensor-memory-operand MMAs",
+             "back to back beside 8 warps of FMA / exp2 arithmetic (2 per SM sub-partition)")
     st = h3.stream_ptr()
-    for mode in range(4):
+    for mode in range(5):
         h3.h3_diag_issue_rate(mode, 200, sms, st)  # warm-up
         vals = sorted(h3.h3_diag_issue_rate(mode, 2000, sms, st) for _ in range(max(reps, 1)))
         dev, site = h3.h3_last_device_error(st)

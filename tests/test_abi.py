@@ -140,7 +140,7 @@ def test_more_invalid_arguments_rejected_before_launch(h3mod):
     assert L.h3_kernel_timer_start(-1) == h3mod.H3_EINVAL
     # the issue-rate diagnostic: mode, batch count, CTA count and output are range-checked
     out = ctypes.c_double(0.0)
-    assert L.h3_diag_issue_rate(4, 10, 1, ctypes.byref(out), None) == h3mod.H3_EINVAL
+    assert L.h3_diag_issue_rate(5, 10, 1, ctypes.byref(out), None) == h3mod.H3_EINVAL
     assert L.h3_diag_issue_rate(-1, 10, 1, ctypes.byref(out), None) == h3mod.H3_EINVAL
     assert L.h3_diag_issue_rate(0, 0, 1, ctypes.byref(out), None) == h3mod.H3_EINVAL
     assert L.h3_diag_issue_rate(0, 10, 0, ctypes.byref(out), None) == h3mod.H3_EINVAL

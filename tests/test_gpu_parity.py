@@ -678,7 +678,7 @@ def test_issue_rate_diagnostic_issues_its_mmas():
     """h3_diag_issue_rate really runs its MMAs: no mode can beat the tensor pipe's full rate of
     64 cycles per 128x128x16 MMA, every CTA finishes, and the error word stays clear."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for mode in range(4):
+    for mode in range(5):
         c = h3.h3_diag_issue_rate(mode, 100, sms, h3.stream_ptr())
         assert 60.0 <= c < 1000.0, (mode, c)
     sync_ok()
