@@ -37,13 +37,17 @@ def test_distribution():
 
 
 def test_layouts_and_sizes():
-    for name, n in [("tiny", 72), ("block1829", 1829), ("block12936", 12936), ("trunk33720", 33720)]:
+    for name, n in [("tiny", 72), ("block1829", 1829), ("block12936", 12936), ("trunk33720", 33720),
+                    ("trunk50x1829_narrow", 1829)]:
         cfg = synth.CONFIGS[name]
         tag, tidx, pos = synth.packed_rows(cfg)
         assert len(tag) == n and pos.shape == (n, 3)
         assert set(np.unique(tag)) <= {0, 1, 2}
         assert tidx.min() >= 0 and tidx.max() < cfg.n_timesteps
     assert len(synth.CONFIGS["trunk33720"].timesteps) == 77
+    narrow = synth.CONFIGS["trunk50x1829_narrow"]
+    assert narrow.dims.head_dim == synth.H3.head_dim and narrow.dims.rope_sections == synth.H3.rope_sections
+    assert narrow.n_blocks == 50 and len(narrow.timesteps) == 77
     tag, tidx, pos = synth.packed_rows(synth.CONFIGS["trunk33720"], step=5)
     assert len(np.unique(tidx)) == 2  # video and audio schedules differ away from sigma = 1
 
