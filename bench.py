@@ -18,6 +18,7 @@ bounded sample of the same workload, on rank 0.
 from __future__ import annotations
 
 import argparse
+import functools
 import json
 import os
 import statistics
@@ -149,18 +150,12 @@ class ClockSampler:
 # ------------------------------------------------------------------------------ CPU oracle leg
 
 
-def cpu_oracle_sample(cfg, rows=CPU_SAMPLE_ROWS, step=10):
-    """Time the CPU oracle on one full-width block over `rows` rows sampled from the packed
-    sequence (same tags, positions and timestep mix), then scale by the FLOP model to the
-    whole trunk.  Returns (tokens/s, seconds, threads, description)."""
+@functools.lru_cache(maxsize=2)
+def _oracle_inputs(cfg, rows, step):
+    """The sampled rows' inputs for the oracle leg, drawn once per process (generating a
+    full-width block's weights takes longer than the timed block forward itself)."""
     import oracle.h3_oracle as O
 
-    try:
-        from threadpoolctl import threadpool_info
-
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        threads = os.cpu_count() or 1
     tag, tidx, pos = synth.packed_rows(cfg, step=step)
     sel = np.sort(np.random.default_rng(0).choice(cfg.layout.n_rows, rows, replace=False))
     sub = synth.Config(cfg.name + "_sample", cfg.dims, cfg.layout, cfg.seed, timesteps=cfg.timesteps,
@@ -173,8 +168,25 @@ def cpu_oracle_sample(cfg, rows=CPU_SAMPLE_ROWS, step=10):
     _, tbf = O.modcache(temb, [aw], [ab])
     remap = {int(t): i for i, t in enumerate(used)}
     tl = np.array([remap[int(t)] for t in tidx[sel]], np.int32)
+    return x, w, tbf[:, 0, :], tag[sel], tl, pos[sel]
+
+
+def cpu_oracle_sample(cfg, rows=CPU_SAMPLE_ROWS, step=10):
+    """Time the CPU oracle on one full-width block over `rows` rows sampled from the packed
+    sequence (same tags, positions and timestep mix), then scale by the FLOP model to the
+    whole trunk.  Returns (tokens/s, seconds, threads, description)."""
+    import oracle.h3_oracle as O
+
+    try:
+        from threadpoolctl import threadpool_info
+
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        threads = os.cpu_count() or 1
+    rows = min(rows, cfg.layout.n_rows)
+    x, w, tb, tag, tl, pos = _oracle_inputs(cfg, rows, step)
     t0 = time.perf_counter()
-    O.block_forward(x, w, tbf[:, 0, :], tag[sel], tl, pos[sel], cfg.dims)
+    O.block_forward(x, w, tb, tag, tl, pos, cfg.dims)
     dt = time.perf_counter() - t0
     lin_s, att_s = _flops(cfg, rows)
     rate = (lin_s + att_s) / dt

@@ -83,3 +83,25 @@ def test_clock_samples_flag_a_thermal_slowdown(tmp_path):
     cs.proc = _Done()
     cs.f = open(path, "a")
     assert cs.stop()["reasons"] == ["hw_thermal_slowdown"]
+
+
+def test_reference_arm_line(capsys):
+    """The reference arm (the CPU oracle, rank 0 only) prints one line with the contract's keys;
+    on the 72-row configuration it finishes in well under a second."""
+    import argparse
+    import json
+
+    import synth
+
+    args = argparse.Namespace(gpus=1, steps=2, warmup=1)
+    bench.run_reference(args, synth.CONFIGS["tiny"], 0)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] == 1 and line["higher_is_better"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "tiny"
+    # other ranks print nothing
+    bench.run_reference(args, synth.CONFIGS["tiny"], 1)
+    assert capsys.readouterr().out == ""
