@@ -207,6 +207,12 @@ CONFIGS = {
         "trunk50x1829_narrow", NARROW, Layout(256, (), 37, (6, 16, 16)), seed=5, n_blocks=50, n_timesteps=77,
         timesteps=_T77,
     ),
+    # the H3 geometry at full width, 50 blocks deep, over block1829's packed rows: the trunk's
+    # error growth along the residual stream at the real width and magnitudes
+    "trunk50x1829": Config(
+        "trunk50x1829", H3, Layout(256, (), 37, (6, 16, 16)), seed=6, n_blocks=50, n_timesteps=77,
+        timesteps=_T77,
+    ),
     "trunk33720": Config(
         "trunk33720", H3, Layout(256, (24, 42), 200, (32, 24, 42)), seed=4, n_blocks=50, n_timesteps=77,
         timesteps=_T77,

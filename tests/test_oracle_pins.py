@@ -528,3 +528,131 @@ def test_euler_integrates_a_constant_velocity_exactly():
         z = O.euler_step(z, v, sig[i], sig[i + 1])
     np.testing.assert_allclose(z, z0 + (sig[-1] - sig[0]) * v, rtol=0, atol=1e-12)
     np.testing.assert_array_equal(O.euler_step(z0, v, 0.5, 0.5), z0)
+
+
+def test_shifted_sigmas_hand_worked_values():
+    """Hand-worked points of the shift s sigma / (1 + (s - 1) sigma) ("minimax-h3-mlx" README,
+    "AdaLN precompute": video shift 12.0, audio shift 3.0).  On a 4-step grid sigma runs
+    1, 0.75, 0.5, 0.25, 0, and every point below is one correctly rounded float32 division of
+    exact operands:
+      shift 3:  0.75 -> 2.25 / 2.5 = 0.9;   0.5 -> 1.5 / 2 = 0.75;  0.25 -> 0.75 / 1.5 = 0.5
+      shift 12: 0.75 -> 9 / 9.25 = 36/37;   0.5 -> 6 / 6.5 = 12/13;  0.25 -> 3 / 3.75 = 0.8
+    A plausible slip such as sigma^(1/s) gives 0.794 / 0.976 at sigma = 0.5 instead."""
+    f32 = np.float32
+    np.testing.assert_array_equal(O.shifted_sigmas(4, 3.0), np.array([1, 0.9, 0.75, 0.5, 0], np.float32))
+    np.testing.assert_array_equal(O.shifted_sigmas(4, 12.0),
+                                  np.array([1, f32(36 / 37), f32(12 / 13), f32(0.8), 0], np.float32))
+    np.testing.assert_array_equal(O.shifted_sigmas(2, 12.0)[1], f32(12 / 13))
+
+
+@pytest.mark.parametrize("shift", [3.0, 12.0, 5.5])
+def test_shifted_sigmas_equal_the_exponential_time_shift(shift):
+    """The same grid written as the exponential time shift of rectified-flow samplers ("Layout":
+    Euler with an exponential sigma shift): sigma' = e^mu / (e^mu + (1/sigma - 1)) with
+    mu = ln s.  Evaluated here in float64 from that form; the oracle's float32 result must sit
+    within two float32 ulps of it at every interior grid point."""
+    steps = 40
+    sig = O.linspace_f32(1.0, 0.0, steps + 1).astype(np.float64)[1:-1]
+    mu = math.log(shift)
+    want = math.exp(mu) / (math.exp(mu) + (1.0 / sig - 1.0))
+    got = O.shifted_sigmas(steps, shift).astype(np.float64)[1:-1]
+    ulp = np.spacing(want.astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(got - want) <= 2 * ulp), np.max(np.abs(got - want) / ulp)
+
+
+def _wiring_case():
+    """A small packed sequence [text 3 | cond 2x2 | audio 5 | video 1x2x3] with every gate of
+    every block zero, so the trunk is exactly the identity (the residual branches add 0)."""
+    d = synth.Dims(hidden=128, heads=4, head_dim=32, ffn=128, temb_dim=16)
+    cfg = synth.Config("wiring", d, synth.Layout(3, (2, 2), 5, (1, 2, 3)), seed=21, n_blocks=2)
+    lay = cfg.layout
+    n = lay.n_rows
+    tag, _, pos = synth.packed_rows(cfg)
+    tidx = np.arange(n, dtype=np.int32)  # one table row per packed row
+    H = d.hidden
+    rng = np.random.default_rng(22)
+    table = rng.standard_normal((n, cfg.n_blocks, 18 * H))
+    t4 = table.reshape(n, cfg.n_blocks, 18, H)
+    t4[:, :, [2, 5, 8, 11, 14, 17], :] = 0.0  # gate_msa, gate_mlp of every tag
+    blocks = [synth.block_weights(cfg, b) for b in range(cfg.n_blocks)]
+    text_x = O.round_bf16(rng.standard_normal((lay.text, H)))
+    return cfg, d, tag, tidx, pos, table, blocks, text_x
+
+
+def _wiring_io(H, kv, ka):
+    return {k: np.zeros(s, np.float32) for k, s in (
+        ("patch_v", (H, kv)), ("patch_v_b", (H,)), ("patch_a", (H, ka)), ("patch_a_b", (H,)),
+        ("head_v", (kv, H)), ("head_v_b", (kv,)), ("head_a", (ka, H)), ("head_a_b", (ka,)))}
+
+
+def test_denoise_step_exit_wiring_closed_form():
+    """Which head, which rows and which d sigma: with the final scale at -1 every row's head
+    input is its final shift alone, and with one table row per packed row (tidx = r) and shift
+    (r + 1)(tag + 1) in every channel, selector heads (output k reads channel k) with biases
+    0.5 (audio) and 0.25 (video) give, for packed row r of a segment,
+      z_new = z + dsigma_seg ((r + 1)(tag + 1) + b_seg).
+    Worked out here, not by the oracle's own steps; swapping the heads, the segment offsets,
+    the tags or the two d sigma values changes the result."""
+    cfg, d, tag, tidx, pos, table, blocks, text_x = _wiring_case()
+    lay, H, n = cfg.layout, d.hidden, cfg.layout.n_rows
+    kv, ka = synth.VIDEO_FEATURES, synth.AUDIO_FEATURES
+    io = _wiring_io(H, kv, ka)
+    io["head_v"][np.arange(kv), np.arange(kv)] = 1.0
+    io["head_a"][np.arange(ka), np.arange(ka)] = 1.0
+    io["head_v_b"][:] = 0.25
+    io["head_a_b"][:] = 0.5
+    table_f = np.zeros((n, 6 * H))
+    tf = table_f.reshape(n, 3, 2, H)
+    for r in range(n):
+        for tg in range(3):
+            tf[r, tg, 0, :] = (r + 1) * (tg + 1)  # shift
+            tf[r, tg, 1, :] = -1.0                # scale: (1 + scale) = 0
+    rng = np.random.default_rng(23)
+    zc = rng.standard_normal((lay.n_cond, kv))
+    za = rng.standard_normal((lay.audio, ka))
+    zv = rng.standard_normal((lay.n_video, kv))
+    ds_v, ds_a = -0.0625, -0.125
+    za2, zv2 = O.denoise_step(text_x, zc, za, zv, io, blocks, table, table_f, tag, tidx, pos, d, ds_v, ds_a)
+    a0 = lay.text + lay.n_cond
+    v0 = a0 + lay.audio
+    ra = np.arange(a0, v0)[:, None]
+    rv = np.arange(v0, n)[:, None]
+    assert np.all(tag[a0:v0] == synth.TAG_AUDIO) and np.all(tag[v0:] == synth.TAG_VIDEO)
+    np.testing.assert_allclose(za2, za + ds_a * ((ra + 1) * (synth.TAG_AUDIO + 1) + 0.5), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(zv2, zv + ds_v * ((rv + 1) * (synth.TAG_VIDEO + 1) + 0.25), rtol=0, atol=1e-12)
+
+
+def test_denoise_step_entry_wiring_closed_form():
+    """Which patch projection and which rows: the entry weights write channels 0 and 1 of a
+    row's latent as the hidden pattern [z0, -z0, z1, -z1, ...] (exact in bf16 for the eighths
+    drawn here), whose LayerNorm is worked out by hand -- mean 0, variance (z0^2 + z1^2) / 2 --
+    so with zero final modulation and heads reading hidden channels 0 and 2 the row's velocity
+    is (z0, z1) / sqrt((z0^2 + z1^2) / 2 + eps) in its first two outputs and 0 elsewhere.
+    A latent row embedded at another row's place, or a segment read from the wrong offset,
+    breaks it (the condition rows carry other latents)."""
+    cfg, d, tag, tidx, pos, table, blocks, text_x = _wiring_case()
+    lay, H, n = cfg.layout, d.hidden, cfg.layout.n_rows
+    kv, ka = synth.VIDEO_FEATURES, synth.AUDIO_FEATURES
+    io = _wiring_io(H, kv, ka)
+    c = np.arange(H)
+    sign = np.where(c % 2 == 0, 1.0, -1.0)
+    for pw in (io["patch_v"], io["patch_a"]):
+        pw[c, (c // 2) % 2] = sign  # hidden c reads latent channel (c // 2) % 2 with sign (-1)^c
+    for hw in (io["head_v"], io["head_a"]):
+        hw[0, 0] = 1.0
+        hw[1, 2] = 1.0
+    table_f = np.zeros((n, 6 * H))
+    rng = np.random.default_rng(24)
+    eighths = lambda shape: rng.integers(-24, 25, shape) / 8.0  # noqa: E731
+    zc, za, zv = eighths((lay.n_cond, kv)), eighths((lay.audio, ka)), eighths((lay.n_video, kv))
+    za[:, :2] = np.where(za[:, :2] == 0, 0.5, za[:, :2])
+    zv[:, :2] = np.where(zv[:, :2] == 0, 0.5, zv[:, :2])
+    ds_v, ds_a = -0.0625, -0.125
+    eps = d.ln_eps
+    za2, zv2 = O.denoise_step(text_x, zc, za, zv, io, blocks, table, table_f, tag, tidx, pos, d, ds_v, ds_a)
+    for z, z2, ds in ((za, za2, ds_a), (zv, zv2, ds_v)):
+        den = np.sqrt((z[:, 0] ** 2 + z[:, 1] ** 2) / 2.0 + eps)
+        want = z.copy()
+        want[:, 0] += ds * z[:, 0] / den
+        want[:, 1] += ds * z[:, 1] / den
+        np.testing.assert_allclose(z2, want, rtol=0, atol=1e-12)
