@@ -48,23 +48,20 @@ def _peaks():
 
 
 def _attention_traffic(n_rows):
-    """DRAM bytes per attention launch at n_rows, from the ncu capture summarised in
-    profiles/attention_tc_kernel_12936x56.md, scaled by rows (Q, K, V and O are each read or
-    written once per launch while K/V tiles stay L2-resident, so traffic grows with N); None
-    when the kernel source has changed since that capture."""
+    """DRAM bytes per attention launch at n_rows, from the ncu capture recorded in
+    profiles/attention_traffic.json, scaled by rows (Q, K, V and O are each read or written once
+    per launch while K/V tiles stay L2-resident, so traffic grows with N); None when there is no
+    capture or the kernel source has changed since it was taken."""
     import hashlib
-    import re
 
     try:
-        text = open(os.path.join(ROOT, "profiles", "attention_tc_kernel_12936x56.md")).read()
-        m = re.search(r"traffic_bytes_per_launch=(\d+) rows=(\d+) source_sha256=([0-9a-f]{64})", text)
-        if not m:
+        with open(os.path.join(ROOT, "profiles", "attention_traffic.json")) as f:
+            rec = json.load(f)
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
             return None
-        src = open(os.path.join(ROOT, "joint_video_audio_block_b300", "csrc", "attention.cu"), "rb").read()
-        if hashlib.sha256(src).hexdigest() != m.group(3):
-            return None
-        return int(m.group(1)) * n_rows / int(m.group(2))
-    except OSError:
+        return int(rec["traffic_bytes_per_launch"]) * n_rows / int(rec["rows"])
+    except (OSError, KeyError, ValueError):
         return None
 
 

@@ -214,6 +214,8 @@ h3_status h3_linear_forward(const h3_linear* lin, int epilogue, const void* x, i
  * given), then rotate-half RoPE with angle pos[r][axis(i)] * theta^(-2i/hd) for pair (i, i+hd/2),
  * axis(i) by rope_sections.  Outputs head-major q_out, k_out: device bf16 [nh][n_rows][hd];
  * vt_out: device bf16 [nh][hd][ld_vt] (v transposed, ld_vt >= n_rows, ld_vt % 8 == 0).
+ * qkv, q_out, k_out, vt_out and workspace must be 16-byte aligned, pos 4-byte aligned;
+ * anything else returns H3_EINVAL before a launch.
  * workspace: device scratch of >= n_rows * hd/2 * 8 bytes (the per-row cos/sin table). */
 h3_status h3_qknorm_rope(const h3_dims* dims, const void* qkv, const float* pos, const void* q_norm,
                          const void* k_norm, void* q_out, void* k_out, void* vt_out, int ld_vt, int n_rows,
@@ -260,7 +262,8 @@ h3_status h3_attention_sparse(const h3_dims* dims, const void* q, const void* k,
  *   n_rows * head_dim / 2 > H3_QKROPE_STATIC_MAX_PAIRS (32768 rows at head_dim 128, 65536 at
  *   64) returns H3_EINVAL before any launch; so do the argument errors of h3_qknorm_rope.
  * The first call on a device looks up the array's device address (once per device, with that
- * device current); make that first call before any stream capture.  Every call shares the
+ * device current) and caches it; make that first call before any stream capture.  The cached
+ * address does not survive cudaDeviceReset (the library's module is reloaded afterwards).  Every call shares the
  * array: calls whose GPU work overlaps (different streams without ordering) race on it and
  * must be serialised by the caller.  Each call rewrites the part it reads, so the array needs
  * no clearing. */
@@ -286,23 +289,6 @@ h3_status h3_kernel_timer_read(float* ms, int capacity, int* n_recorded);
  * reports H3_ETIMEOUT with that site and the context stays usable.  No fault or trap is
  * involved.  timeout_us outside the range returns H3_EINVAL. */
 h3_status h3_diag_expire_wait(unsigned timeout_us, void* stream);
-
-/* Diagnostic of the tensor pipe as one issuing thread feeds it (no counterpart on the pages:
- * it measures the hardware property the attention and GEMM pipelines are designed around).
- * Launches `ctas` CTAs (1 .. H3_DIAG_MAX_CTAS; one per SM fits), each issuing `batches`
- * (1 .. 100,000) batches of 16 bf16 MMAs of 128x128x16 (8 with both operands in shared memory,
- * 8 with A in tensor memory) on whatever the memories hold; nothing is read back.
- * mode 0: back to back; 1: between the shared-memory-operand and the tensor-memory-operand
- * MMAs of each batch the issuing thread polls an mbarrier whose phase is already complete and
- * uses the answer at once; 2: the same poll as a non-blocking test read after the batch;
- * 3: the blocking poll after the batch instead; 4: mode 0 while eight more warps, two per SM
- * sub-partition, run dependent FMA / exp2 arithmetic (mode outside 0..4: H3_EINVAL).
- * Synchronises `stream` and writes to the host
- * double *cycles_per_mma the median over CTAs of SM cycles per MMA (64 at full rate).  The
- * per-CTA counts live in a fixed array inside the library (no allocation).  A wait that runs
- * out is reported by h3_last_device_error (site 0x302). */
-#define H3_DIAG_MAX_CTAS 1024
-h3_status h3_diag_issue_rate(int mode, int batches, int ctas, double* cycles_per_mma, void* stream);
 
 /* Synchronises `stream`, then reads and clears the device error word.  Returns H3_OK, or
  * H3_ETIMEOUT when a bounded device wait ran out since the last call (*site, if not NULL,

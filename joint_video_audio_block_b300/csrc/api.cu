@@ -14,6 +14,7 @@
 // Activation arenas follow their lifetimes inside the block ("H3-metal" README, "Scheduling
 // and activation memory"): the QKV arena is reused for the SwiGLU activation, and the
 // attention-branch output x' is written straight into x_out.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <vector>
@@ -28,16 +29,20 @@ __device__ unsigned g_error_word;  // first error site recorded by a bounded dev
 unsigned* error_word();
 unsigned* h3_error_word_ptr() { return error_word(); }
 
+// Device address of g_error_word on the current device, looked up once per device and cached
+// (host threads may race on the first lookup; they all store the same address).
 unsigned* error_word() {
-  static unsigned* ptr[64] = {nullptr};
+  static std::atomic<unsigned*> ptr[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptr[dev]) {
+  unsigned* w = ptr[dev].load(std::memory_order_acquire);
+  if (!w) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    ptr[dev] = static_cast<unsigned*>(p);
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess || !p) return nullptr;
+    w = static_cast<unsigned*>(p);
+    ptr[dev].store(w, std::memory_order_release);
   }
-  return ptr[dev];
+  return w;
 }
 
 static size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -97,6 +102,22 @@ static bool dims_ok(const h3_dims* d) {
   const int* s = d->rope_sections;
   if (s[0] < 0 || s[1] < 0 || s[2] < 0 || s[0] + s[1] + s[2] != d->head_dim / 2) return false;
   if (!(d->rope_theta > 0.f) || !(d->ln_eps >= 0.f) || !(d->qk_eps >= 0.f)) return false;
+  return true;
+}
+
+// Host checks shared by h3_qknorm_rope and h3_qknorm_rope_static: the geometry, null pointers,
+// and the alignment qknorm_rope_kernel's vector accesses need -- qkv, q_out and k_out 16 bytes
+// (8-byte word loads / stores per lane at head_dim 128), vt_out 16 bytes with ld_vt % 8 == 0
+// (16-byte transposed stores), pos 4 bytes, the norm weights 2 bytes.
+bool qknorm_rope_args_ok(const h3_dims* d, const void* qkv, const float* pos, const void* q_norm,
+                         const void* k_norm, const void* q_out, const void* k_out, const void* vt_out, int ld_vt,
+                         int n_rows) {
+  if (!dims_ok(d) || !qkv || !pos || !q_out || !k_out || !vt_out || n_rows < 0) return false;
+  if (ld_vt < n_rows || ld_vt % 8 || ((q_norm == nullptr) != (k_norm == nullptr))) return false;
+  if (!aligned16(qkv) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(vt_out)) return false;
+  if ((reinterpret_cast<uintptr_t>(pos) & 3) || (reinterpret_cast<uintptr_t>(q_norm) & 1) ||
+      (reinterpret_cast<uintptr_t>(k_norm) & 1))
+    return false;
   return true;
 }
 
@@ -311,8 +332,7 @@ h3_status h3_linear_forward(const h3_linear* lin, int epilogue, const void* x, i
 h3_status h3_qknorm_rope(const h3_dims* dims, const void* qkv, const float* pos, const void* q_norm,
                          const void* k_norm, void* q_out, void* k_out, void* vt_out, int ld_vt, int n_rows,
                          void* workspace, size_t ws_bytes, void* stream) {
-  if (!dims_ok(dims) || !qkv || !pos || !q_out || !k_out || !vt_out || n_rows < 0 || !workspace) return H3_EINVAL;
-  if (ld_vt < n_rows || ld_vt % 8 || !aligned16(vt_out) || ((q_norm == nullptr) != (k_norm == nullptr)))
+  if (!qknorm_rope_args_ok(dims, qkv, pos, q_norm, k_norm, q_out, k_out, vt_out, ld_vt, n_rows) || !workspace)
     return H3_EINVAL;
   const size_t need = static_cast<size_t>(n_rows) * (dims->head_dim / 2) * sizeof(float2);
   if (ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15)) return H3_EINVAL;

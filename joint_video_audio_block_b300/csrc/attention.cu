@@ -119,9 +119,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const uint32_t b_sfull = b_kvempty + 8 * ST;    // [2] (tile A, tile B)
   const uint32_t b_pfull = b_sfull + 16;          // [2]
   const uint32_t b_odone = b_pfull + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + 3 * ST + 5);
+  const uint32_t b_drain = b_odone + 8;           // failure path: the issuer's MMAs have completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + 3 * ST + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ErrCtx ec = err_ctx(err);
   const int h = blockIdx.y;
   const int q0 = blockIdx.x * 2 * AT_BM;
   const int nt = cdiv(n_rows, AT_BN);
@@ -153,6 +155,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(b_pfull + 8 * x, 4);
     }
     mbar_init(b_odone, 1);
+    mbar_init(b_drain, 1);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -181,15 +184,28 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       for (int x = 0; x < 2; ++x)
         for (int a = 0; a < HD / 64; ++a)
           tma_load_3d(sQ + x * C::QK_TILE + a * AT_ATOM, &tmQ, b_q, 64 * a, q0 + x * AT_BM, h);
+      int issued = 0;
+      bool ok = true;
       for (int it = 0, j = next_tile(0); j < nt; ++it, j = next_tile(j + 1)) {
         const int s = it % ST;
-        if (!mbar_wait(b_kvempty + 8 * s, ((it / ST) & 1) ^ 1, err, kErrAttnProducer)) break;
+        if (!mbar_wait(b_kvempty + 8 * s, ((it / ST) & 1) ^ 1, ec, kErrAttnProducer)) {
+          ok = false;
+          break;
+        }
         const uint32_t kd = sK + s * C::QK_TILE, vd = sV + s * C::V_TILE;
         mbar_arrive_expect_tx(b_kfull + 8 * s, C::QK_TILE);
         for (int a = 0; a < HD / 64; ++a) tma_load_3d(kd + a * AT_ATOM, &tmK, b_kfull + 8 * s, 64 * a, j * AT_BN, h);
         mbar_arrive_expect_tx(b_vfull + 8 * s, C::V_TILE);
         tma_load_3d(vd, &tmV, b_vfull + 8 * s, j * AT_BN, 0, h);
         tma_load_3d(vd + C::V_ATOM, &tmV, b_vfull + 8 * s, j * AT_BN + 64, 0, h);
+        issued = it + 1;
+      }
+      if (!ok) {  // let the copies still in flight land before the shared memory is released
+        mbar_drain(b_q, 0);
+        for (int i = issued > ST ? issued - ST : 0; i < issued; ++i) {
+          mbar_drain(b_kfull + 8 * (i % ST), (i / ST) & 1);
+          mbar_drain(b_vfull + 8 * (i % ST), (i / ST) & 1);
+        }
       }
     }
   } else if (warp == 1) {
@@ -218,9 +234,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // after PV_x of the current one, so it may overwrite P_x in TMEM (in-order execution).
       int j = next_tile(0);
       int cnt[2] = {0, 0};
-      bool ok = mbar_wait(b_q, 0, err, kErrAttnMma);
+      bool ok = mbar_wait(b_q, 0, ec, kErrAttnMma);
       if (ok && j < nt) {
-        ok = mbar_wait(b_kfull, 0, err, kErrAttnMma);
+        ok = mbar_wait(b_kfull, 0, ec, kErrAttnMma);
         if (ok) {
           tc_fence_after();
           if (keep(0, j)) issue_s(0, 0);
@@ -236,11 +252,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (keep(x, j)) {  // P_x V for this tile
-            if (!mbar_wait(b_pfull + 8 * x, cnt[x] & 1, err, kErrAttnMma)) {
+            if (!mbar_wait(b_pfull + 8 * x, cnt[x] & 1, ec, kErrAttnMma)) {
               ok = false;
               break;
             }
-            if (!v_ready && !mbar_wait(b_vfull + 8 * s, par, err, kErrAttnMma)) {
+            if (!v_ready && !mbar_wait(b_vfull + 8 * s, par, ec, kErrAttnMma)) {
               ok = false;
               break;
             }
@@ -251,7 +267,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           }
           if (x == 1) umma_commit(b_kvempty + 8 * s);  // K / V of this stage are no longer read
           if (more && keep(x, jn)) {  // S_x of the next visited tile
-            if (!k_ready && !mbar_wait(b_kfull + 8 * ((it + 1) % ST), ((it + 1) / ST) & 1, err, kErrAttnMma)) {
+            if (!k_ready && !mbar_wait(b_kfull + 8 * ((it + 1) % ST), ((it + 1) / ST) & 1, ec, kErrAttnMma)) {
               ok = false;
               break;
             }
@@ -262,7 +278,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         j = jn;
       }
-      if (ok) umma_commit(b_odone);
+      if (ok) {
+        umma_commit(b_odone);
+      } else {  // the MMAs already issued finish before TMEM is released
+        umma_commit(b_drain);
+        mbar_drain(b_drain, 0);
+      }
     }
   } else if (warp >= 4) {
     // softmax warps: tile x = 0 (warps 4..7) or 1 (warps 8..11); TMEM lane quadrant = warp % 4
@@ -278,7 +299,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     int cnt = 0;  // S / P phases of this query tile = key tiles it keeps
     for (int j = next_tile(0); j < nt; j = next_tile(j + 1)) {
       if (SPARSE && !keep(x, j)) continue;  // visited for the other query tile only
-      if (!mbar_wait(b_sfull + 8 * x, cnt & 1, err, kErrAttnSoftmax)) {
+      if (!mbar_wait(b_sfull + 8 * x, cnt & 1, ec, kErrAttnSoftmax)) {
         ok = false;
         break;
       }
@@ -352,7 +373,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pfull + 8 * x);
     }
-    if (ok && mbar_wait(b_odone, 0, err, kErrAttnSoftmax)) {
+    if (ok && mbar_wait(b_odone, 0, ec, kErrAttnSoftmax)) {
       tc_fence_after();
       const int row = q0 + x * AT_BM + r;
       const float inv = l > 0.f ? 1.f / l : 0.f;  // a row that kept no key tile outputs zeros

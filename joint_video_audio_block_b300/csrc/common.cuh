@@ -2,9 +2,10 @@
 // bounded waits, TMA tensor loads, and the tcgen05 (UMMA + TMEM) instruction wrappers.
 //
 // Every wait on an mbarrier is bounded: after kWaitTimeoutNs of global time (or as soon as
-// another CTA has reported an error) the wait returns false, the caller records a site code
-// in the library's device error word, leaves its loop and reaches the kernel's teardown, so a
-// broken pipeline ends the launch instead of hanging the GPU.
+// another CTA of the launch has reported an error) the wait returns false, the caller records
+// a site code in the library's device error word, lets the copies and MMAs it already issued
+// complete (mbar_drain), leaves its loop and reaches the kernel's teardown, so a broken
+// pipeline ends the launch instead of hanging the GPU.
 #pragma once
 
 #include <cuda.h>
@@ -82,21 +83,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The device error word as one launch sees it: its address and the value it held when the
+// thread started.  A wait gives up early only when the word has changed since then, i.e. when
+// another CTA of this launch has reported; a report left by an earlier launch (not yet read by
+// h3_last_device_error) does not cut this launch short.
+struct ErrCtx {
+  unsigned* word;
+  unsigned seen;
+};
+__device__ __forceinline__ ErrCtx err_ctx(unsigned* w) {
+  return ErrCtx{w, w ? *reinterpret_cast<volatile unsigned*>(w) : 0u};
+}
+
 // Wait until the phase with the given parity has completed.  Returns false (after recording
-// `site`) on timeout or when another CTA has already reported an error.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err, unsigned site,
+// `site`) on timeout or when another CTA of the launch has reported an error meanwhile.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const ErrCtx& e, unsigned site,
                                           unsigned long long timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 1023u) == 0) {
-      if (err && *reinterpret_cast<volatile unsigned*>(err) != 0u) return false;
+      if (e.word && *reinterpret_cast<volatile unsigned*>(e.word) != e.seen) return false;
       if (globaltimer() - t0 > timeout_ns) {
-        record_error(err, site);
+        record_error(e.word, site);
         return false;
       }
     }
+  }
+}
+
+// Failure-path drain: wait (bounded, reporting nothing) until a phase that asynchronous work
+// already issued will complete -- a TMA copy landing, a tcgen05.commit arriving -- so that a
+// CTA leaving its loop early frees its shared and tensor memory only once nothing is still
+// writing them.
+constexpr unsigned long long kDrainTimeoutNs = 200000000ull;  // 200 ms
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 1023u) == 1023u && globaltimer() - t0 > kDrainTimeoutNs) return;
   }
 }
 

@@ -20,7 +20,7 @@ __global__ void expire_wait_kernel(unsigned long long timeout_ns, unsigned* err)
   }
   __syncthreads();
   // phase 0 never completes: no thread arrives
-  const bool ok = mbar_wait(b, 0, err, kErrDiagWait, timeout_ns);
+  const bool ok = mbar_wait(b, 0, err_ctx(err), kErrDiagWait, timeout_ns);
   (void)ok;
   __syncthreads();
 }

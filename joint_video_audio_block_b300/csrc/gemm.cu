@@ -447,8 +447,10 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
   const uint32_t bar_ready = bar_empty + 8 * S;      // S barriers: INT8 dequant done
   const uint32_t bar_tfull = bar_ready + 8 * S;      // 2 barriers: accumulator complete
   const uint32_t bar_tempty = bar_tfull + 16;        // 2 barriers: accumulator drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 4);
+  const uint32_t bar_drain = bar_tempty + 16;        // failure path: the issuer's MMAs have completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ErrCtx ec = err_ctx(p.err);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -460,6 +462,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       mbar_init(bar_tfull + 8 * a, 1);
       mbar_init(bar_tempty + 8 * a, 4);
     }
+    mbar_init(bar_drain, 1);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int s = 0;
+      int s = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
@@ -488,8 +491,8 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
         tile_coords(tile, p.m_tiles, p.n_tiles, p.group_m, mb, nb);
         int brow0, brow1;
         b_tile_rows<EPI>(p, nb, brow0, brow1);
-        for (int kb = 0; kb < p.kb_count; ++kb) {
-          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, p.err, kErrGemmProducer)) {
+        for (int kb = 0; kb < p.kb_count; ++kb, ++issued) {
+          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ec, kErrGemmProducer)) {
             ok = false;
             break;
           }
@@ -508,6 +511,8 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
           }
         }
       }
+      if (!ok)  // let the copies still in flight land before the shared memory is released
+        for (int i = issued > S ? issued - S : 0; i < issued; ++i) mbar_drain(bar_full + 8 * (i % S), (i / S) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -516,12 +521,15 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       uint32_t ph = 0, aph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1, p.err, kErrGemmMma)) break;
+        if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1, ec, kErrGemmMma)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * C::MSUB * G_BN;  // accumulator a of the tile at d + a * 256
         for (int kb = 0; kb < p.kb_count; ++kb) {
-          if (!mbar_wait(bar_full + 8 * s, ph, p.err, kErrGemmMma) ||
-              (INT8 && !mbar_wait(bar_ready + 8 * s, ph, p.err, kErrGemmMma))) {
+          if (!mbar_wait(bar_full + 8 * s, ph, ec, kErrGemmMma) ||
+              (INT8 && !mbar_wait(bar_ready + 8 * s, ph, ec, kErrGemmMma))) {
             ok = false;
             break;
           }
@@ -546,6 +554,10 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
           aph ^= 1;
         }
       }
+      if (!ok) {  // the MMAs already issued finish before TMEM is released
+        umma_commit(bar_drain);
+        mbar_drain(bar_drain, 0);
+      }
     }
   } else if (warp < 6) {
     const int quad = warp & 3;
@@ -554,7 +566,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int mb, nb;
       tile_coords(tile, p.m_tiles, p.n_tiles, p.group_m, mb, nb);
-      if (!mbar_wait(bar_tfull + 8 * acc, aph, p.err, kErrGemmEpilogue)) break;
+      if (!mbar_wait(bar_tfull + 8 * acc, aph, ec, kErrGemmEpilogue)) break;
       tc_fence_after();
 #pragma unroll 1
       for (int a = 0; a < C::MSUB; ++a) {
@@ -613,7 +625,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     // refill d three stages ahead
     auto stage = [&](DqStage& d) {
       if (!ok || cur.tile >= p.num_tiles) return;
-      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, p.err, kErrGemmDequant)) {
+      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ec, kErrGemmDequant)) {
         ok = false;
         return;
       }

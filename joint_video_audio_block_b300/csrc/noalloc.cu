@@ -11,6 +11,8 @@
 // Sharing: every call (on any stream) writes the same array.  Calls whose GPU work overlaps
 // race on it; the caller must order them (one stream, or events).  The table is fully
 // rewritten for the rows a call uses before it is read, so no part needs to start at zero.
+#include <atomic>
+
 #include "../../include/h3.h"
 #include "kernels.h"
 
@@ -21,18 +23,26 @@ static __device__ __align__(256) float2 g_rope_scratch[H3_QKROPE_STATIC_MAX_PAIR
 
 // Device address of g_rope_scratch on the current device.  In host code the array's name is
 // only a host-side stand-in, so the address is looked up once per device (with that device
-// current) and cached.  Returns nullptr if the lookup fails.
+// current) and cached; host threads may race on the first lookup and all store the same
+// address.  Returns nullptr if the lookup fails.
 static float2* rope_scratch_ptr() {
-  static float2* ptr[64] = {nullptr};
+  static std::atomic<float2*> ptr[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptr[dev]) {
+  float2* a = ptr[dev].load(std::memory_order_acquire);
+  if (!a) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_rope_scratch) != cudaSuccess || !p) return nullptr;
-    ptr[dev] = static_cast<float2*>(p);
+    a = static_cast<float2*>(p);
+    ptr[dev].store(a, std::memory_order_release);
   }
-  return ptr[dev];
+  return a;
 }
+
+// argument checks shared with h3_qknorm_rope (api.cu)
+bool qknorm_rope_args_ok(const h3_dims* d, const void* qkv, const float* pos, const void* q_norm,
+                         const void* k_norm, const void* q_out, const void* k_out, const void* vt_out, int ld_vt,
+                         int n_rows);
 
 }  // namespace h3
 
@@ -41,17 +51,9 @@ using namespace h3;
 extern "C" h3_status h3_qknorm_rope_static(const h3_dims* dims, const void* qkv, const float* pos,
                                            const void* q_norm, const void* k_norm, void* q_out, void* k_out,
                                            void* vt_out, int ld_vt, int n_rows, void* stream) {
-  if (!dims || !qkv || !pos || !q_out || !k_out || !vt_out || n_rows < 0) return H3_EINVAL;
-  if (dims->head_dim != 64 && dims->head_dim != 128) return H3_EINVAL;
-  if (ld_vt < n_rows || ld_vt % 8 || (reinterpret_cast<uintptr_t>(vt_out) & 15) ||
-      ((q_norm == nullptr) != (k_norm == nullptr)))
-    return H3_EINVAL;
+  if (!qknorm_rope_args_ok(dims, qkv, pos, q_norm, k_norm, q_out, k_out, vt_out, ld_vt, n_rows)) return H3_EINVAL;
   const long long pairs = static_cast<long long>(n_rows) * (dims->head_dim / 2);
   if (pairs > H3_QKROPE_STATIC_MAX_PAIRS) return H3_EINVAL;  // beyond the fixed scratch array
-  const int* s = dims->rope_sections;
-  if (dims->heads <= 0 || s[0] < 0 || s[1] < 0 || s[2] < 0 || s[0] + s[1] + s[2] != dims->head_dim / 2 ||
-      !(dims->rope_theta > 0.f) || !(dims->qk_eps >= 0.f))
-    return H3_EINVAL;
   if (n_rows == 0) return H3_OK;
   float2* cs = rope_scratch_ptr();
   if (!cs) return H3_ECUDA;

@@ -25,13 +25,11 @@ EXPORTS = (
     "h3_linear_forward", "h3_qknorm_rope", "h3_qknorm_rope_static", "h3_attention", "h3_last_device_error",
     "h3_status_str", "h3_kernel_timer_start", "h3_kernel_timer_read", "h3_qkv_project",
     "h3_qkv_project_workspace_size", "h3_diag_expire_wait", "h3_attention_sparse", "h3_embed_rows",
-    "h3_final_modcache_build", "h3_head_forward", "h3_sigma_schedule", "h3_denoise_step", "h3_diag_issue_rate",
+    "h3_final_modcache_build", "h3_head_forward", "h3_sigma_schedule", "h3_denoise_step",
 )
 
 # largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
 H3_QKROPE_STATIC_MAX_PAIRS = 1 << 21
-# most CTAs h3_diag_issue_rate launches
-H3_DIAG_MAX_CTAS = 1024
 
 
 class H3Error(RuntimeError):
@@ -97,7 +95,6 @@ def lib():
             "h3_last_device_error": (i32, [vp, ctypes.POINTER(u32)]),
             "h3_kernel_timer_start": (i32, [i32]),
             "h3_diag_expire_wait": (i32, [u32, vp]),
-            "h3_diag_issue_rate": (i32, [i32, i32, i32, ctypes.POINTER(ctypes.c_double), vp]),
             "h3_kernel_timer_read": (i32, [ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(i32)]),
             "h3_status_str": (ctypes.c_char_p, [i32]),
         }
@@ -196,16 +193,6 @@ def h3_kernel_timer_read(capacity: int) -> list:
 
 def h3_diag_expire_wait(timeout_us: int, stream):
     _check(lib().h3_diag_expire_wait(timeout_us, stream), "h3_diag_expire_wait")
-
-
-def h3_diag_issue_rate(mode: int, batches: int, ctas: int, stream) -> float:
-    """SM cycles per 128x128x16 MMA as one thread issues them: mode 0 back to back, 1 with a
-    barrier poll between the 8 shared-memory-operand and 8 tensor-memory-operand MMAs of each
-    batch, 2 with that poll as a test read after the batch, 3 with the poll after the batch, 4
-    back to back beside eight warps of FMA / exp2 arithmetic; synchronises the stream."""
-    out = ctypes.c_double(0.0)
-    _check(lib().h3_diag_issue_rate(mode, batches, ctas, ctypes.byref(out), stream), "h3_diag_issue_rate")
-    return out.value
 
 
 def h3_attention_sparse(dims, q, k, vt, ld_vt, o, n_rows, tile_mask, stream):

@@ -30,7 +30,7 @@ from joint_video_audio_block_b300 import h3  # noqa: E402
 from joint_video_audio_block_b300 import runtime as R  # noqa: E402
 
 KERNELS = ("block", "attention", "attention_sparse", "qkv", "o", "fc1", "fc2", "adaln", "qkrope", "qkvrope",
-           "modcache", "embed", "head", "issue_rate")
+           "modcache", "embed", "head")
 
 
 def _normal(shape, std=1.0, mean=0.0, stream=1):
@@ -240,29 +240,6 @@ def setup(kernel: str, n: int, int8: bool, density: float = 0.25):
     raise ValueError(kernel)
 
 
-def issue_rate(reps: int):
-    """The tensor pipe fed by one issuing thread (h3_diag_issue_rate), one CTA per SM, 2,000
-    batches of 16 MMAs of 128x128x16 per CTA (8 with shared-memory operands, then 8 with A in
-    tensor memory): back to back, with a barrier poll between the two halves, with that poll as
-    a test read after the batch, with the poll after the batch, and back to back while eight more
-    warps run arithmetic beside the issuer.  Prints one line per mode
-    with the median cycles per MMA over `reps` launches (64 = full rate)."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    names = ("back to back", "blocking poll after the shared-memory-operand MMAs",
-             "test there, answer read after the batch", "blocking poll after the tensor-memory-operand MMAs",
-             "back to back beside 8 warps of FMA / exp2 arithmetic (2 per SM sub-partition)")
-    st = h3.stream_ptr()
-    for mode in range(5):
-        h3.h3_diag_issue_rate(mode, 200, sms, st)  # warm-up
-        vals = sorted(h3.h3_diag_issue_rate(mode, 2000, sms, st) for _ in range(max(reps, 1)))
-        dev, site = h3.h3_last_device_error(st)
-        if dev != h3.H3_OK:
-            raise RuntimeError(f"device error word set: site {site:#x}")
-        c = vals[len(vals) // 2]
-        print(json.dumps({"kernel": "issue_rate", "mode": mode, "what": names[mode], "ctas": sms,
-                          "cycles_per_mma": c, "of_full_rate": 64.0 / c}), flush=True)
-
-
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel", choices=KERNELS, required=True)
@@ -273,8 +250,6 @@ def main(argv=None):
     ap.add_argument("--density", type=float, default=0.25, help="attention_sparse: fraction of kept tiles")
     a = ap.parse_args(argv)
     torch.cuda.set_device(0)
-    if a.kernel == "issue_rate":
-        issue_rate(a.reps)
         return
     launch, flop, byts, note, _keep = setup(a.kernel, a.rows, a.int8, a.density)
     for _ in range(a.warmup):

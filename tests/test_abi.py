@@ -130,7 +130,7 @@ def test_more_invalid_arguments_rejected_before_launch(h3mod):
     buf = (ctypes.c_float * 4)()
     assert L.h3_sigma_schedule(0, ctypes.c_float(3.0), buf) == h3mod.H3_EINVAL
     assert L.h3_sigma_schedule(3, ctypes.c_float(0.0), buf) == h3mod.H3_EINVAL
-    # the static-scratch variant refuses sizes beyond its array, and the diagnostic its range
+    # the static-scratch variant refuses sizes beyond its array, and the wait diagnostic its range
     n = h3mod.H3_QKROPE_STATIC_MAX_PAIRS // 32 + 1  # head_dim 64 -> 32 pairs per row
     assert L.h3_qknorm_rope_static(ctypes.byref(d), al, al, None, None, al, al, al, (n + 63) // 64 * 64, n,
                                    None) == h3mod.H3_EINVAL
@@ -138,11 +138,41 @@ def test_more_invalid_arguments_rejected_before_launch(h3mod):
     assert L.h3_diag_expire_wait(2_000_000, None) == h3mod.H3_EINVAL
     # the timer: negative capacity
     assert L.h3_kernel_timer_start(-1) == h3mod.H3_EINVAL
-    # the issue-rate diagnostic: mode, batch count, CTA count and output are range-checked
-    out = ctypes.c_double(0.0)
-    assert L.h3_diag_issue_rate(5, 10, 1, ctypes.byref(out), None) == h3mod.H3_EINVAL
-    assert L.h3_diag_issue_rate(-1, 10, 1, ctypes.byref(out), None) == h3mod.H3_EINVAL
-    assert L.h3_diag_issue_rate(0, 0, 1, ctypes.byref(out), None) == h3mod.H3_EINVAL
-    assert L.h3_diag_issue_rate(0, 10, 0, ctypes.byref(out), None) == h3mod.H3_EINVAL
-    assert L.h3_diag_issue_rate(0, 10, h3mod.H3_DIAG_MAX_CTAS + 1, ctypes.byref(out), None) == h3mod.H3_EINVAL
-    assert L.h3_diag_issue_rate(0, 10, 1, None, None) == h3mod.H3_EINVAL
+
+
+def test_qknorm_rope_entry_points_refuse_misaligned_pointers(h3mod):
+    """Both QK-norm + RoPE entry points refuse, on the host, any pointer the kernel would access
+    with a vector width it is not aligned to (qkv, q_out, k_out, vt_out: 16 bytes; pos: 4), and
+    the allocation-free one refuses the same geometry errors as the workspace one."""
+    L = h3mod.lib()
+    d = _tiny_dims(h3mod)
+    al, ws = 0x10000, 0x20000
+    n, ld = 0, 128  # zero rows: a valid call returns H3_OK right after its checks, launching nothing
+    base = [al, al, None, None, al, al, al, ld, n]
+
+    def call(args, static):
+        qkv, pos, qn, kn, q, k, vt, ldv, rows = args
+        if static:
+            return L.h3_qknorm_rope_static(ctypes.byref(d), qkv, pos, qn, kn, q, k, vt, ldv, rows, None)
+        return L.h3_qknorm_rope(ctypes.byref(d), qkv, pos, qn, kn, q, k, vt, ldv, rows, ws, 1 << 20, None)
+
+    for static in (False, True):
+        assert call(base, static) == h3mod.H3_OK
+        for slot, off in ((0, 2), (0, 8), (4, 2), (4, 8), (5, 4), (5, 8), (6, 8), (1, 2)):
+            bad = list(base)
+            bad[slot] = al + off
+            assert call(bad, static) == h3mod.H3_EINVAL, (static, slot, off)
+        bad = list(base)
+        bad[7] = 76  # ld_vt not a multiple of 8
+        assert call(bad, static) == h3mod.H3_EINVAL
+        bad = list(base)
+        bad[2] = al  # one norm weight without the other
+        assert call(bad, static) == h3mod.H3_EINVAL
+    # geometry the workspace entry point refuses is refused by the static one too
+    for field, value in (("n_tags", 0), ("hidden", 0), ("ln_eps", -1.0)):
+        dd = h3mod.make_dims(192, 4, 64, 512, (8, 12, 12))
+        setattr(dd, field, value)
+        assert L.h3_qknorm_rope_static(ctypes.byref(dd), al, al, None, None, al, al, al, ld, n, None) == \
+            h3mod.H3_EINVAL
+        assert L.h3_qknorm_rope(ctypes.byref(dd), al, al, None, None, al, al, al, ld, n, ws, 1 << 20, None) == \
+            h3mod.H3_EINVAL

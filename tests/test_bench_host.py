@@ -20,11 +20,14 @@ def test_max_over_ranks_without_a_group_is_identity():
 
 
 def _fake_tree(tmp_path, src: bytes, sha: str, bytes_, rows):
+    import json
+
     (tmp_path / "profiles").mkdir()
     (tmp_path / "joint_video_audio_block_b300" / "csrc").mkdir(parents=True)
     (tmp_path / "joint_video_audio_block_b300" / "csrc" / "attention.cu").write_bytes(src)
-    (tmp_path / "profiles" / "attention_tc_kernel_12936x56.md").write_text(
-        f"summary\n\ntraffic_bytes_per_launch={bytes_} rows={rows} source_sha256={sha}\n")
+    (tmp_path / "profiles" / "attention_traffic.json").write_text(json.dumps({
+        "rows": rows, "traffic_bytes_per_launch": bytes_, "source_sha256": sha,
+        "source": "joint_video_audio_block_b300/csrc/attention.cu"}))
 
 
 def test_attention_traffic_scales_by_rows_when_the_source_matches(tmp_path, monkeypatch):
@@ -46,9 +49,14 @@ def test_attention_traffic_is_null_without_a_capture(tmp_path, monkeypatch):
     assert bench._attention_traffic(100) is None
 
 
-def test_committed_capture_line_is_well_formed():
-    text = open(os.path.join(bench.ROOT, "profiles", "attention_tc_kernel_12936x56.md")).read()
-    assert "traffic_bytes_per_launch=" in text and "source_sha256=" in text
+def test_committed_capture_record_is_well_formed():
+    import json
+
+    with open(os.path.join(bench.ROOT, "profiles", "attention_traffic.json")) as f:
+        rec = json.load(f)
+    assert rec["rows"] > 0 and rec["traffic_bytes_per_launch"] > 0 and len(rec["source_sha256"]) == 64
+    assert os.path.exists(os.path.join(bench.ROOT, rec["source"]))
+    assert "--clock-control none" in rec["command"]
 
 
 class _Done:
