@@ -219,6 +219,70 @@ def run_reference(args, cfg, rank):
 # ------------------------------------------------------------------------------ GPU arm
 
 
+BLOCK_WORKLOADS = ("block1829", "block12936", "block12936_int8")
+
+
+def time_single_blocks(dev, sp, reps=20, warmup=5):
+    """One full-width DiT block (h3_block_forward) per configuration: 1,829 and 12,936 packed
+    rows with bf16 weights, and 12,936 rows with weight-only INT8-g32 weights.  Device-drawn
+    weights (seeded), the block's table built by h3_modcache_build, CUDA events around `reps`
+    back-to-back launches after `warmup`; the block's 0.77 GB of weights (0.43 GB as INT8)
+    exceed L2, so every launch streams them from HBM."""
+    import torch
+
+    from joint_video_audio_block_b300 import h3
+    from joint_video_audio_block_b300 import runtime as R
+
+    _, bf16_peak, _, peak_kind = _peaks()
+    out = {}
+    for name in BLOCK_WORKLOADS:
+        cfg = synth.CONFIGS[name]
+        d = cfg.dims
+        dims = R.dims_of(d)
+        N = cfg.layout.n_rows
+        w = synth.device_block_weights(cfg, 0)
+        if cfg.int8:
+            for lname in ("wqkv", "wo", "w1", "w2"):
+                w[lname], w[lname + "_scale"], w[lname + "_qbias"] = synth.device_quantize_int8_g32(w[lname])
+        bw = h3.make_block_w(w)
+        aw, ab = synth.device_adaln_weights(cfg, 0)
+        temb = torch.from_numpy(synth.temb(cfg)).to(dev)
+        T = temb.shape[0]
+        table = torch.empty(T, 1, 18 * d.hidden, dtype=torch.bfloat16, device=dev)
+        h3.h3_modcache_build(dims, temb.data_ptr(), T, d.temb_dim, [aw.data_ptr()], [ab.data_ptr()], 1,
+                             table.data_ptr(), sp)
+        del aw, ab
+        tag, tidx, pos = (torch.from_numpy(a).to(dev) for a in synth.packed_rows(cfg))
+        x = synth.device_normal_bf16(cfg.seed, 0xFFFF02, (N, d.hidden))
+        y = torch.empty_like(x)
+        ws = R.workspace(dims, N)
+
+        def launch():
+            h3.h3_block_forward(dims, bw, table.data_ptr(), 18 * d.hidden, T, x.data_ptr(), y.data_ptr(), N,
+                                tag.data_ptr(), tidx.data_ptr(), pos.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp)
+
+        for _ in range(warmup):
+            launch()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            launch()
+        e1.record()
+        torch.cuda.synchronize()
+        st, site = h3.h3_last_device_error(sp)
+        if st != h3.H3_OK:
+            raise RuntimeError(f"device error timing {name}: site {site:#x}")
+        ms = e0.elapsed_time(e1) / reps
+        lin, att = _flops(cfg, N)
+        out[name] = {"rows": N, "weights": "int8_g32" if cfg.int8 else "bf16", "ms_per_block": ms,
+                     "tflops": (lin + att) / ms / 1e9, "frac_of_burst": (lin + att) / ms / 1e9 / bf16_peak,
+                     "ms_at_60pct_of_burst": (lin + att) / (0.6 * bf16_peak * 1e12) * 1e3, "reps": reps,
+                     "peak_kind": peak_kind}
+        del w, bw, table, x, y, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, cfg, rank, world, local_rank):
     import torch
 
@@ -369,6 +433,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     mma_tflops = B * (lin_f + att_f) / (ms_per_step / 1e3) / 1e12  # per GPU (each replica)
     traffic = _attention_traffic(N)
 
+    blocks_timed = None if args.no_block_workloads else time_single_blocks(dev, sp)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt, threads, desc = cpu_oracle_sample(cfg)
@@ -395,6 +461,7 @@ def run_ours(args, cfg, rank, world, local_rank):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "sampler_transition": {"ms": transition_ms, "tokens_per_s": N / (transition_ms / 1e3),
                                    "what": "entry projections + trunk + output heads + Euler (h3_denoise_step)"},
+            "single_block_workloads": blocks_timed,
             "gpu_launches": args.steps * (1 + 7 * B),  # rope table + 7 kernels per block
             "clocks": clk,
             "cpu_baseline": cpu,
@@ -413,6 +480,8 @@ def main():
     ap.add_argument("--workload", default="trunk33720")
     ap.add_argument("--blocks", type=int, default=0, help="override the block count (diagnostics only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-block-workloads", action="store_true",
+                    help="skip the per-block timings of the 1,829- and 12,936-row configurations")
     ap.add_argument("--clocks-csv", default=None, help="where to keep the raw clock samples ({rank} is replaced)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))

@@ -96,7 +96,9 @@ size_t h3_workspace_size(const h3_dims* dims, int n_rows);
 /* a0 -- ModulationCache build ("minimax-h3-mlx" README, "AdaLN precompute").
  *   table[t][b][j] = bf16( sum_k adaln_w[b][j][k] * temb[t][k] + adaln_b[b][j] ),
  * fp32 accumulation, j < 18*H.
- * temb: device f32 [T, Dt]; adaln_w: HOST array of n_blocks device pointers (16-byte aligned) to bf16 [18H, Dt];
+ * On the tensor cores: temb splits exactly into three bf16 terms and the three products
+ * accumulate in fp32, so every product is exact and only the fp32 accumulation rounds.
+ * temb: device f32 [T, Dt], 16-byte aligned; adaln_w: HOST array of n_blocks device pointers (16-byte aligned) to bf16 [18H, Dt];
  * adaln_b: HOST array of n_blocks device pointers to bf16 [18H] (array or entries may be NULL);
  * table: device bf16 [T][n_blocks][18H], written.  Dt % 8 == 0. */
 h3_status h3_modcache_build(const h3_dims* dims, const float* temb, int T, int Dt, const void* const* adaln_w,
@@ -134,7 +136,8 @@ h3_status h3_embed_rows(const h3_dims* dims, const float* z, int K, const float*
                         void* x_rows, void* stream);
 
 /* Final-layer modulation table: table_f[t][j] = bf16(sum_k w[j][k] temb[t][k] + b[j]),
- * j < 6H, read as 3 modality tags x (shift, scale) x H.  temb: device f32 [T, Dt]; w: device
+ * j < 6H, read as 3 modality tags x (shift, scale) x H (the kernel of h3_modcache_build).
+ * temb: device f32 [T, Dt], 16-byte aligned; w: device
  * bf16 [6H, Dt] (16-byte aligned); b: device bf16 [6H] or NULL; table_f: device bf16 [T][6H]. */
 h3_status h3_final_modcache_build(const h3_dims* dims, const float* temb, int T, int Dt, const void* w, const void* b,
                                   void* table_f, void* stream);

@@ -280,19 +280,18 @@ h3_status h3_last_device_error(void* stream, unsigned* site) {
 
 h3_status h3_modcache_build(const h3_dims* dims, const float* temb, int T, int Dt, const void* const* adaln_w,
                             const void* const* adaln_b, int n_blocks, void* table, void* stream) {
-  if (!dims_ok(dims) || !temb || T <= 0 || Dt <= 0 || Dt % 8 || !adaln_w || n_blocks <= 0 || !table)
+  if (!dims_ok(dims) || !temb || !aligned16(temb) || T <= 0 || Dt <= 0 || Dt % 8 || !adaln_w || n_blocks <= 0 ||
+      !table)
     return H3_EINVAL;
+  for (int b = 0; b < n_blocks; ++b)
+    if (!adaln_w[b] || !aligned16(adaln_w[b]) || (adaln_b && adaln_b[b] && (reinterpret_cast<uintptr_t>(adaln_b[b]) & 1)))
+      return H3_EINVAL;
   const int n_out = 18 * dims->hidden;
   const long long t_stride = static_cast<long long>(n_blocks) * n_out;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  for (int b = 0; b < n_blocks; ++b) {
-    if (!adaln_w[b] || !aligned16(adaln_w[b])) return H3_EINVAL;
-    const bf16* bias = adaln_b ? static_cast<const bf16*>(adaln_b[b]) : nullptr;
-    cudaError_t e = launch_modcache(temb, T, Dt, static_cast<const bf16*>(adaln_w[b]), bias, n_out,
-                                    static_cast<bf16*>(table) + static_cast<long long>(b) * n_out, t_stride, st);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
-  return H3_OK;
+  return cuda_status(launch_modcache(temb, T, Dt, reinterpret_cast<const bf16* const*>(adaln_w),
+                                     reinterpret_cast<const bf16* const*>(adaln_b), n_blocks, n_out,
+                                     static_cast<bf16*>(table), t_stride, error_word(),
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 h3_status h3_adaln_modulate(const h3_dims* dims, const void* x, void* xn, int n_rows, const void* table_b,

@@ -24,6 +24,7 @@ enum ErrSite : unsigned {
   kErrGemmProducer = 0x101, kErrGemmMma = 0x102, kErrGemmEpilogue = 0x103, kErrGemmDequant = 0x104,
   kErrAttnProducer = 0x201, kErrAttnMma = 0x202, kErrAttnSoftmax = 0x203,
   kErrDiagWait = 0x301,  // the diagnostic wait of h3_diag_expire_wait
+  kErrModcacheProducer = 0x401, kErrModcacheMma = 0x402, kErrModcacheEpilogue = 0x403, kErrModcacheSplit = 0x404,
 };
 
 __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }

@@ -243,12 +243,15 @@ extern "C" h3_status h3_head_forward(const h3_dims* dims, const void* x_rows, in
 
 extern "C" h3_status h3_final_modcache_build(const h3_dims* dims, const float* temb, int T, int Dt, const void* w,
                                              const void* b, void* table_f, void* stream) {
-  if (!dims || !temb || !w || !table_f || T <= 0 || Dt <= 0 || Dt % 8 || !a16(w)) return H3_EINVAL;
+  if (!dims || !temb || !a16(temb) || !w || !table_f || T <= 0 || Dt <= 0 || Dt % 8 || !a16(w)) return H3_EINVAL;
   const int n_out = 6 * dims->hidden;
   if (dims->hidden <= 0 || dims->hidden % 64) return H3_EINVAL;
-  const cudaError_t e = launch_modcache(temb, T, Dt, static_cast<const bf16*>(w), static_cast<const bf16*>(b), n_out,
-                                        static_cast<bf16*>(table_f), n_out, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? H3_OK : H3_ECUDA;
+  const bf16* wp = static_cast<const bf16*>(w);
+  const bf16* bp = static_cast<const bf16*>(b);
+  const cudaError_t e = launch_modcache(temb, T, Dt, &wp, &bp, 1, n_out, static_cast<bf16*>(table_f), n_out,
+                                        h3_error_word_ptr(), static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) return H3_OK;
+  return e == cudaErrorInvalidValue ? H3_EINVAL : H3_ECUDA;
 }
 
 // float32 linspace the way the scheduler's reference evaluates it (a float32 step; the first

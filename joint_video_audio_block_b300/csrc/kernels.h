@@ -60,8 +60,11 @@ cudaError_t launch_rope_table(const float* pos, float2* cs, int n_rows, int hd, 
 cudaError_t launch_qknorm_rope(const bf16* qkv, const float2* cs, const bf16* qn, const bf16* kn, float eps, bf16* q,
                                bf16* k, bf16* vt, int ld_vt, int n_rows, int nh, int hd, cudaStream_t st);
 
-cudaError_t launch_modcache(const float* temb, int T, int Dt, const bf16* W, const bf16* bias, int n_out,
-                            bf16* table_b, long long t_stride, cudaStream_t st);
+// table[t * t_stride + b * n_out + j] = bf16(W[b][j] . temb[t] + bias[b][j]) for b < n_blocks
+// (bias may be null, or hold null entries); temb 16-byte aligned, Dt % 8 == 0.
+cudaError_t launch_modcache(const float* temb, int T, int Dt, const bf16* const* W, const bf16* const* bias,
+                            int n_blocks, int n_out, bf16* table, long long t_stride, unsigned* err,
+                            cudaStream_t st);
 
 cudaError_t launch_linear_ref(const LinearArgs& a, cudaStream_t st);
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st);

@@ -37,7 +37,7 @@ def _normal(shape, std=1.0, mean=0.0, stream=1):
     return synth.device_normal_bf16(7, stream, shape, mean, std)
 
 
-def setup(kernel: str, n: int, int8: bool, density: float = 0.25):
+def setup(kernel: str, n: int, int8: bool, density: float = 0.25, blocks: int = 1):
     """Returns (launch(), flop, bytes, note) for one launch of `kernel` over n rows."""
     d = synth.H3
     H, I, F, hd, nh = d.hidden, d.inner, d.ffn, d.head_dim, d.heads
@@ -226,16 +226,18 @@ def setup(kernel: str, n: int, int8: bool, density: float = 0.25):
     if kernel == "modcache":
         T = n
         temb = torch.from_numpy(synth.sinusoidal_temb(list(range(T)), d.temb_dim)).cuda()
-        W, b = _normal((18 * H, d.temb_dim), 0.02, stream=16), _normal((18 * H,), 0.02, stream=17)
-        table = torch.empty(T, 1, 18 * H, dtype=torch.bfloat16, device="cuda")
-        keep += [temb, W, b, table]
+        Ws = [_normal((18 * H, d.temb_dim), 0.02, stream=16 + 2 * i) for i in range(blocks)]
+        bs = [_normal((18 * H,), 0.02, stream=17 + 2 * i) for i in range(blocks)]
+        table = torch.empty(T, blocks, 18 * H, dtype=torch.bfloat16, device="cuda")
+        keep += [temb, table] + Ws + bs
 
         def launch():
-            h3.h3_modcache_build(dims, temb.data_ptr(), T, d.temb_dim, [W.data_ptr()], [b.data_ptr()], 1,
-                                 table.data_ptr(), st)
+            h3.h3_modcache_build(dims, temb.data_ptr(), T, d.temb_dim, [W.data_ptr() for W in Ws],
+                                 [b.data_ptr() for b in bs], blocks, table.data_ptr(), st)
 
-        byts = 18.0 * H * d.temb_dim * 2 + T * d.temb_dim * 4 + T * 18 * H * 2
-        return launch, 2.0 * T * 18 * H * d.temb_dim, byts, "rows = timesteps T; one block's adaln_proj", keep
+        byts = blocks * (18.0 * H * d.temb_dim * 2 + 18 * H * 2) + T * d.temb_dim * 4 + T * blocks * 18 * H * 2
+        return (launch, 2.0 * T * blocks * 18 * H * d.temb_dim, byts,
+                f"rows = timesteps T; {blocks} blocks' adaln_proj", keep)
 
     raise ValueError(kernel)
 
@@ -248,10 +250,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--int8", action="store_true")
     ap.add_argument("--density", type=float, default=0.25, help="attention_sparse: fraction of kept tiles")
+    ap.add_argument("--blocks", type=int, default=1, help="modcache: blocks whose tables one call builds")
     a = ap.parse_args(argv)
     torch.cuda.set_device(0)
-        return
-    launch, flop, byts, note, _keep = setup(a.kernel, a.rows, a.int8, a.density)
+    launch, flop, byts, note, _keep = setup(a.kernel, a.rows, a.int8, a.density, a.blocks)
     for _ in range(a.warmup):
         launch()
     torch.cuda.synchronize()

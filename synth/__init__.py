@@ -440,3 +440,21 @@ def device_adaln_weights(cfg: Config, block: int, device="cuda"):
     W = device_normal_bf16(s, _stream(block, _T_AW), (18 * d.hidden, d.temb_dim), 0.0, 0.02, device)
     b = device_normal_bf16(s, _stream(block, _T_AB), (18 * d.hidden,), 0.0, 0.02, device)
     return W, b
+
+
+def device_quantize_int8_g32(w):
+    """quantize_int8_g32 applied with torch ops to a device bf16 tensor [Nout, K] (benchmark
+    weights only; the same recipe: per group of 32 along K, scale = bf16((hi - lo) / 255),
+    qbias = bf16(lo), q = clamp(round_half_even((w - qbias) / scale), 0, 255), q = 0 where the
+    scale is 0).  Returns (q u8, scale bf16, qbias bf16) device tensors."""
+    import torch
+
+    n, k = w.shape
+    g = w.float().view(n, k // 32, 32)
+    lo, hi = g.amin(dim=2), g.amax(dim=2)
+    scale = ((hi - lo) / 255.0).to(torch.bfloat16)
+    qb = lo.to(torch.bfloat16)
+    sf, qf = scale.float()[:, :, None], qb.float()[:, :, None]
+    t = torch.where(sf == 0, torch.zeros_like(g), (g - qf) / torch.where(sf == 0, torch.ones_like(sf), sf))
+    q = torch.clamp(torch.round(t), 0, 255).to(torch.uint8)
+    return q.view(n, k).contiguous(), scale.contiguous(), qb.contiguous()

@@ -28,18 +28,51 @@ def _err(gpu, ref):
     return np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300), float(np.abs(gpu - ref).max())
 
 
-def check(gpu, ref, rel=REL_L2, abs_=MAX_ABS, what=""):
-    """Block-output tolerance: relative L2 <= 1e-2 and max-abs <= 5e-2, both relative to the
-    reference's own norm (L2 and max).  Read this way because these inputs give block outputs
-    up to |x| ~ 66, where adjacent bf16 values are 0.25-0.5 apart: an absolute 5e-2 is below
-    the spacing of the output format itself.  The bf16 floor is pinned separately where a test
-    also runs the bf16-storage oracle (GPU error <= 2x that oracle's error)."""
+def _per_element(err, ref):
+    """|gpu - ref| in units of the plain per-element reading of the bound, 5e-2 max(1, |ref|)."""
+    return np.abs(err) / (MAX_ABS * np.maximum(1.0, np.abs(ref)))
+
+
+def check(gpu, ref, emu=None, rel=REL_L2, abs_=MAX_ABS, what=""):
+    """Block-output tolerance (stated for a bf16 block output against the fp32/fp64 oracle):
+    relative L2 <= 1e-2 and max-abs <= 5e-2.
+
+    - Relative L2 over the whole output: <= 1e-2.
+    - Max-abs, per token: every element of a row within 5e-2 max(1, max|ref[row, :]|), the
+      row's own scale (these synthetic blocks give rows with max|x| between ~26 and ~66).
+    - Max-abs, per element, |gpu - ref| <= 5e-2 max(1, |ref|): where the test also has the
+      oracle run with bf16 storage at the GPU's rounding points (`emu`), the GPU may exceed
+      this plain reading only as far as that oracle does -- measured on the 1,829-row block,
+      the bf16-storage oracle itself exceeds it at 0.42% of elements, by up to 4.7x (an output
+      near 0.5 inherits the bf16 rounding of the SwiGLU activation and of x', whose errors
+      scale with the row, not the element) -- so the GPU's worst excess and its count of
+      exceeding elements are each held to 2x the bf16-storage oracle's.  Without `emu` the
+      plain per-element bound must hold outright.
+    - With `emu`, the bf16 floor: GPU relative L2 and max-abs error each <= 2x the
+      bf16-storage oracle's."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
+    ref2 = ref.reshape(ref.shape[0], -1)
+    err2 = (gpu - ref).reshape(ref2.shape)
     r, m = _err(gpu, ref)
-    mr = m / max(float(np.abs(ref).max()), 1e-300)
-    print(f"{what}: rel_l2={r:.3e} max_abs={m:.3e} max_abs/max|ref|={mr:.3e}")
-    assert r <= rel and mr <= abs_, f"{what}: rel_l2={r:.3e} (<= {rel}) max_abs/max|ref|={mr:.3e} (<= {abs_})"
+    row_scale = abs_ * np.maximum(1.0, np.abs(ref2).max(axis=1))
+    per_row = float((np.abs(err2).max(axis=1) / row_scale).max())
+    pe = _per_element(err2, ref2)
+    print(f"{what}: rel_l2={r:.3e} max_abs={m:.3e} per-row max-abs/bound={per_row:.3f} "
+          f"per-element worst={pe.max():.3f} over={np.mean(pe > 1):.2e}")
+    assert r <= rel, f"{what}: rel_l2={r:.3e} (<= {rel})"
+    assert per_row <= 1.0, f"{what}: a row's max-abs error is {per_row:.3f}x 5e-2 of its max|ref|"
+    if emu is None:
+        assert pe.max() <= 1.0, f"{what}: per-element error {pe.max():.3f}x 5e-2 max(1, |ref|)"
+        return
+    emu = np.asarray(emu, np.float64).reshape(ref2.shape)
+    pe_e = _per_element(emu - ref2, ref2)
+    r_e, m_e = _err(emu, ref2)
+    print(f"{what}: bf16-storage oracle rel_l2={r_e:.3e} max_abs={m_e:.3e} per-element worst={pe_e.max():.3f} "
+          f"over={np.mean(pe_e > 1):.2e}")
+    assert pe.max() <= max(1.0, 2 * pe_e.max()), f"{what}: per-element worst {pe.max():.3f} vs {pe_e.max():.3f}"
+    assert np.sum(pe > 1) <= 2 * np.sum(pe_e > 1), f"{what}: {np.sum(pe > 1)} elements over vs {np.sum(pe_e > 1)}"
+    assert r <= 2 * r_e and m <= 2 * m_e, f"{what}: GPU ({r:.3e}, {m:.3e}) vs bf16 floor ({r_e:.3e}, {m_e:.3e})"
 
 
 def check_step(gpu, ref, what="", spread=2e-3, ulps=1, extra=None):
@@ -123,6 +156,33 @@ def test_modcache_build(name, n_blocks):
     excess = np.abs(got - c.table64) - bound
     assert np.all(excess <= 0), excess.max()
     assert np.mean(got == c.table_bf) > 0.99
+
+
+def test_modcache_many_timesteps_and_blocks():
+    """More timesteps than one pass holds (150 = 128 + 22, padded to 32) and more blocks than
+    one launch carries (20 = two groups of 10), with one block's bias absent: every entry
+    within one bf16 ulp (plus the fp32 accumulation bound) of the exact projection."""
+    cfg = synth.CONFIGS["tiny"]
+    d = cfg.dims
+    dims = R.dims_of(d)
+    T, B = 150, 20
+    temb = synth.sinusoidal_temb(np.linspace(999.0, 1.0, T), d.temb_dim)
+    aw = [synth.adaln_weights(cfg, b) for b in range(B)]
+    biases = [None if b == 7 else aw[b][1] for b in range(B)]
+    table64, _ = O.modcache(temb, [w for w, _ in aw], biases)
+    temb_d = torch.from_numpy(temb).cuda()
+    w_d = [R.bf16_from_bits(w) for w, _ in aw]
+    b_d = [None if bb is None else R.bf16_from_bits(bb) for bb in biases]
+    table = torch.empty(T, B, 18 * d.hidden, dtype=torch.bfloat16, device="cuda")
+    h3.h3_modcache_build(dims, temb_d.data_ptr(), T, d.temb_dim, [w.data_ptr() for w in w_d],
+                         [0 if bb is None else bb.data_ptr() for bb in b_d], B, table.data_ptr(), h3.stream_ptr())
+    sync_ok()
+    got = R.f32_from_bf16(table).astype(np.float64)
+    absum = np.stack([np.abs(temb.astype(np.float64)) @ np.abs(O.widen_bf16(w)).T
+                      + (0.0 if bb is None else np.abs(O.widen_bf16(bb))[None]) for (w, _), bb in zip(aw, biases)],
+                     axis=1)
+    excess = np.abs(got - table64) - (2.0 ** -8 * np.abs(table64) + 2.0 ** -20 * absum)
+    assert np.all(excess <= 0), excess.max()
 
 
 # ----------------------------------------------------------------------------- a1 / a6 + gather
@@ -469,7 +529,10 @@ def test_block_tiny(flags):
     if flags & h3.H3_F_NO_QKNORM:
         w.pop("qnorm"), w.pop("knorm")
     ref = O.block_forward(c.x_bits, w, c.table_b(0), c.tag, c.tidx, c.pos, c.d)
-    check(R.f32_from_bf16(out), ref, what=f"block tiny f{flags}")
+    emu = O.block_forward(c.x_bits, w, c.table_b(0), c.tag, c.tidx, c.pos, c.d, emulate_bf16=True)
+    got = R.f32_from_bf16(out)
+    check(got, ref, what=f"block tiny f{flags}")  # the plain per-element reading holds here
+    check(got, ref, emu, what=f"block tiny f{flags} (bf16 floor)")
 
 
 def test_block_in_place_matches_out_of_place():
@@ -501,13 +564,8 @@ def test_block1829_full():
     _run_block(c, wt, c.x, out)
     ref = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d)
     got = R.f32_from_bf16(out)
-    check(got, ref, what="block 1829 rows")
-    # at the bf16 storage floor: no worse than twice the bf16-storage oracle's own distance
     emu = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, emulate_bf16=True)
-    r_e, m_e = _err(emu, ref)
-    r_g, m_g = _err(got, ref)
-    print(f"bf16-storage oracle vs exact: rel_l2={r_e:.3e} max_abs={m_e:.3e}")
-    assert r_g <= 2 * r_e and m_g <= 2 * m_e
+    check(got, ref, emu, what="block 1829 rows")
 
 
 @pytest.mark.parametrize("name", ["block12936", "block12936_int8"])
@@ -523,13 +581,9 @@ def test_block12936_sampled(name):
         deq = {n: O.dequant_int8_g32(*synth.quantize_int8_g32(c.w_bits[0][n])) for n in ("wqkv", "wo", "w1", "w2")}
     ref = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows, dequant=deq)
     got = R.f32_from_bf16(out)[rows]
-    check(got, ref, what=f"{name} sampled")
     emu = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows, dequant=deq,
                           emulate_bf16=True)
-    r_e, m_e = _err(emu, ref)
-    r_g, m_g = _err(got, ref)
-    print(f"bf16-storage oracle vs exact: rel_l2={r_e:.3e} max_abs={m_e:.3e}")
-    assert r_g <= 2 * r_e and m_g <= 2 * m_e
+    check(got, ref, emu, what=f"{name} sampled")
     if int8:
         # report the distance to the bf16 masters (not a tolerance: quantisation error)
         ref_m = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows)
@@ -549,13 +603,9 @@ def test_block33720_sampled():
     rows = np.sort(np.random.default_rng(11).choice(c.n, 256, replace=False))
     ref = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows)
     got = R.f32_from_bf16(out)[rows]
-    check(got, ref, what="block 33720 sampled")
     emu = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows,
                           emulate_bf16=True)
-    r_e, m_e = _err(emu, ref)
-    r_g, m_g = _err(got, ref)
-    print(f"bf16-storage oracle vs exact: rel_l2={r_e:.3e} max_abs={m_e:.3e}")
-    assert r_g <= 2 * r_e and m_g <= 2 * m_e
+    check(got, ref, emu, what="block 33720 sampled")
 
 
 def test_modcache_77_timesteps_full_width():
@@ -638,8 +688,7 @@ def test_trunk_equals_block_sequence():
     r, m = _err(R.f32_from_bf16(x_tr), ref)
     r2, m2 = _err(R.f32_from_bf16(x_tr), ref_e)
     print(f"trunk 3x1829: vs exact rel_l2={r:.3e} max_abs={m:.3e}; vs bf16-storage oracle rel_l2={r2:.3e} max_abs={m2:.3e}")
-    check(R.f32_from_bf16(x_tr), ref, what="trunk 3 blocks")
-    assert r <= 2 * max(_err(ref_e, ref)[0], 1e-3)
+    check(R.f32_from_bf16(x_tr), ref, ref_e, what="trunk 3 blocks")
 
 
 # ----------------------------------------------------------------------------- edges / errors
@@ -695,7 +744,9 @@ def test_unread_error_report_does_not_cut_later_launches_short():
     sync_ok()
     rows = np.sort(np.random.default_rng(3).choice(c.n, 96, replace=False))
     ref = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows)
-    check(R.f32_from_bf16(out)[rows], ref, what="block after an unread report")
+    emu = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, rows=rows,
+                          emulate_bf16=True)
+    check(R.f32_from_bf16(out)[rows], ref, emu, what="block after an unread report")
 
 
 def test_zero_rows_and_bad_arguments():

@@ -1,21 +1,29 @@
-"""GPU parity at full depth: a 50-block trunk through h3_trunk_forward against the oracle.
+"""GPU parity at full depth: 50-block trunks through h3_trunk_forward against the oracle.
 
 The trunk repeats the block 50 times ("minimax-h3-mlx" README, "Architecture"), so rounding
-that is harmless in one block could grow along the residual stream.  This test runs all 50
+that is harmless in one block could grow along the residual stream.  Two tests run all 50
 blocks at 1,829 packed rows with per-row tags and the two timestep indices of a sampling
-step, on the H3 head geometry (128-wide heads, the same rotary split) at a narrower width
-(hidden 1024, 8 heads, SwiGLU 2816): the full-width 50-block oracle takes about ten minutes
-of fp64 on a 16-core host, this one a minute or two.  The kernels, tiles and epilogues it
-exercises are the ones the full-width trunk uses; only the loop trip counts differ.
+step:
+- at full width (hidden 5376, 56 x 128 heads, SwiGLU 14336): every block is checked live on
+  64 sampled rows, and the accumulated output against the exact oracle trunk stored by
+  tests/golden/full_width_trunk.py (two 50-block fp64 chains over every row take about 20
+  minutes, too long to run inside the test);
+- at a narrower width (hidden 1024, 8 x 128 heads, SwiGLU 2816) the oracle trunk runs live,
+  every row of every block checked.
 
-Bars.  The tolerance stated for a block output (relative L2 <= 1e-2, max-abs <= 5e-2 of
-max|ref|) is checked for every one of the 50 blocks, each against the oracle's block applied
-to the same (GPU-produced) input.  For the whole trunk the reference is the exact oracle and
-the bar is the bf16 floor: the GPU's accumulated error may be at most twice that of the oracle
-run with bf16 storage at the GPU's rounding points.  (At this depth bf16 storage at those
-points, with exact arithmetic everywhere else, already moves the output by about 1.7% in
-relative L2, so the per-block bound does not carry over to 50 blocks.)
+Bars.  The tolerance stated for a block output (relative L2 <= 1e-2, max-abs <= 5e-2) is
+checked for every one of the 50 blocks, each against the oracle's block applied to the same
+(GPU-produced) input, max-abs per token (5e-2 of the row's max|ref|).  For the whole trunk the
+reference is the exact oracle and the bar is the bf16 floor: the GPU's accumulated error may
+be at most twice that of the oracle run with bf16 storage at the GPU's rounding points.  (At
+this depth bf16 storage at those points, with exact arithmetic everywhere else, already moves
+the output by percents in relative L2, so the per-block bound does not carry over to 50
+blocks.)
 """
+
+import importlib.util
+import json
+import os
 
 import numpy as np
 import pytest
@@ -37,6 +45,83 @@ def _err(gpu, ref):
     rel = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300)
     mx = float(np.abs(gpu - ref).max()) / max(float(np.abs(ref).max()), 1e-300)
     return rel, mx
+
+
+def _block_err(gpu, ref):
+    """(relative L2, worst per-token max-abs in units of 5e-2 max(1, max|ref[row]|))."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rel = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300)
+    row = np.abs(gpu - ref).max(axis=1) / (5e-2 * np.maximum(1.0, np.abs(ref).max(axis=1)))
+    return rel, float(row.max())
+
+
+def _golden_module():
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "full_width_trunk.py")
+    spec = importlib.util.spec_from_file_location("full_width_trunk", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _device_ok():
+    torch.cuda.synchronize()
+    dev, site = h3.h3_last_device_error(h3.stream_ptr())
+    assert dev == h3.H3_OK, f"device error word set: site {site:#x}"
+
+
+@pytest.mark.slow
+def test_trunk_50_blocks_full_width():
+    G = _golden_module()
+    assert os.path.exists(G.GOLDEN), "stored oracle values missing (run tests/golden/full_width_trunk.py)"
+    cfg, x_bits, tag, tidx, pos, table_bf = G.inputs()
+    d, n, B = cfg.dims, cfg.layout.n_rows, cfg.n_blocks
+    assert B == 50 and d.hidden == 5376 and d.inner == 7168 and d.ffn == 14336
+    assert len(np.unique(tidx)) == 2  # video and audio rows at different timesteps
+    dims = R.dims_of(d)
+    T, H = table_bf.shape[0], d.hidden
+    table = R.bf16_from_bits(O.to_bf16_bits(table_bf))
+    tag_d, tidx_d, pos_d = (torch.from_numpy(a).cuda() for a in (tag, tidx, pos))
+    ws = R.workspace(dims, n)
+    x0 = R.bf16_from_bits(x_bits)
+    rows = np.sort(np.random.default_rng(17).choice(n, 64, replace=False))
+
+    # block by block: every block against the oracle's block on the same (GPU-produced) input
+    wts, xs, worst = [], x0.clone(), (0.0, 0.0, -1)
+    for b in range(B):
+        w = synth.block_weights(cfg, b)
+        wts.append(R.upload_block(w))
+        x_in_bits = O.to_bf16_bits(R.f32_from_bf16(xs))
+        out = torch.empty_like(xs)
+        h3.h3_block_forward(dims, h3.make_block_w(wts[-1]), table.data_ptr() + b * 18 * H * 2, B * 18 * H, T,
+                            xs.data_ptr(), out.data_ptr(), n, tag_d.data_ptr(), tidx_d.data_ptr(), pos_d.data_ptr(),
+                            ws.data_ptr(), ws.numel(), 0, h3.stream_ptr())
+        _device_ok()
+        ref_b = O.block_forward(x_in_bits, w, table_bf[:, b, :], tag, tidx, pos, d, rows=rows)
+        r_b, m_b = _block_err(R.f32_from_bf16(out)[rows], ref_b)
+        assert r_b <= 1e-2 and m_b <= 1.0, f"block {b}: rel_l2={r_b:.3e} per-token max-abs/bound={m_b:.3f}"
+        worst = max(worst, (r_b, m_b, b))
+        xs = out
+    print(f"full width, per-block worst: rel_l2={worst[0]:.3e} per-token max-abs/bound={worst[1]:.3f} "
+          f"(block {worst[2]})")
+
+    # the whole trunk in one call is exactly the 50 block calls
+    x = x0.clone()
+    h3.h3_trunk_forward(dims, [h3.make_block_w(w) for w in wts], B, table.data_ptr(), T, x.data_ptr(), n,
+                        tag_d.data_ptr(), tidx_d.data_ptr(), pos_d.data_ptr(), ws.data_ptr(), ws.numel(), 0,
+                        h3.stream_ptr())
+    _device_ok()
+    assert torch.equal(x, xs)
+
+    # the accumulated error at the bf16 floor, on the stored rows of the exact oracle trunk
+    g = np.load(G.GOLDEN)
+    meta = json.loads(str(g["meta"]))
+    got = R.f32_from_bf16(x)[g["rows"]]
+    r, m = G.rel_errors(got, g["ref"])
+    r_e, m_e = meta["bf16_storage_rel_l2_rows"], meta["bf16_storage_max_abs_rows"]
+    print(f"trunk 50x1829 full width: GPU vs exact rel_l2={r:.3e} max_abs/max|ref|={m:.3e}; "
+          f"bf16-storage oracle vs exact rel_l2={r_e:.3e} max_abs/max|ref|={m_e:.3e}")
+    assert r <= 2 * r_e and m <= 2 * m_e
 
 
 def test_trunk_50_blocks_narrow():
@@ -85,11 +170,11 @@ def test_trunk_50_blocks_narrow():
                             ws.numel(), 0, h3.stream_ptr())
         device_ok()
         ref_b = O.block_forward(x_in_bits, w_bits[b], table_bf[:, b, :], tag, tidx, pos, d)
-        r_b, m_b = _err(R.f32_from_bf16(out), ref_b)
-        assert r_b <= 1e-2 and m_b <= 5e-2, f"block {b}: rel_l2={r_b:.3e} max_abs/max|ref|={m_b:.3e}"
+        r_b, m_b = _block_err(R.f32_from_bf16(out), ref_b)
+        assert r_b <= 1e-2 and m_b <= 1.0, f"block {b}: rel_l2={r_b:.3e} per-token max-abs/bound={m_b:.3f}"
         worst = max(worst, (r_b, m_b, b))
         xs = out
-    print(f"per-block worst: rel_l2={worst[0]:.3e} max_abs/max|ref|={worst[1]:.3e} (block {worst[2]})")
+    print(f"per-block worst: rel_l2={worst[0]:.3e} per-token max-abs/bound={worst[1]:.3f} (block {worst[2]})")
     assert torch.equal(xs, x)  # the trunk call is exactly the 50 block calls
 
     # the accumulated error at the bf16 floor

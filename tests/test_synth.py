@@ -59,3 +59,17 @@ def test_quantizer_codes_in_range():
     # every group uses both ends of the code range
     g = q.reshape(64, 4, 32)
     assert np.all(g.min(axis=2) == 0) and np.all(g.max(axis=2) >= 254)
+
+
+def test_device_quantizer_matches_the_host_recipe():
+    """The torch quantizer that prepares the benchmark's INT8 weights follows the host recipe
+    bit for bit (run here on CPU tensors)."""
+    torch = __import__("pytest").importorskip("torch")
+    w = synth.normal_bf16(3, 2, (96, 256), 0.0, 0.02)
+    w[5, :32] = w[5, 0]  # a constant group: scale 0, every code 0
+    q, s, b = synth.quantize_int8_g32(w)
+    t = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16)
+    qd, sd, bd = synth.device_quantize_int8_g32(t)
+    assert np.array_equal(qd.numpy(), q)
+    assert np.array_equal(sd.view(torch.int16).numpy().view(np.uint16), s)
+    assert np.array_equal(bd.view(torch.int16).numpy().view(np.uint16), b)
