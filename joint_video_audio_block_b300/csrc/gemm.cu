@@ -28,10 +28,12 @@ constexpr int G_BM = 128, G_BN = 256, G_BK = 64;
 constexpr int G_A_BYTES = G_BM * G_BK * 2;   // 16 KB
 constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
 // Tile raster: column sweeps over groups of group_m row-blocks.  The host sizes group_m so a
-// group's A rows (group_m x 128 x K x 2 bytes) take about 48 MB of the 126 MB L2 and stay
+// group's A rows (group_m x 128 x K x 2 bytes) take about 24 MB of the 126 MB L2 and stay
 // resident while the sweep streams B once per group: B is read from HBM m_tiles / group_m
-// times, A once.
-constexpr size_t kRasterABytes = size_t(48) << 20;
+// times, A once.  Measured on fc1 at 33,720 rows (one launch, DRAM bytes read): 5.0 GB with
+// 24 MB groups, 6.4 GB with 48 MB and 19.9 GB with 96 MB, where the larger groups no longer
+// stay resident beside the B stream; the 50-block step time is the same at 24 and 48 MB.
+constexpr size_t kRasterABytes = size_t(24) << 20;
 
 // bf16 weights: 128 x 256 tiles, two TMEM accumulators so the epilogue of one tile overlaps the
 // mainloop of the next.  INT8 weights: 256 x 256 tiles (two 128-row MMAs per k-step share each
@@ -300,7 +302,10 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
           for (int e = 0; e < 8; ++e) {
             const float g = __uint_as_float(rg[8 * q + e]) + bg[e];
             const float u = __uint_as_float(rv[8 * q + e]) + bv[e];
-            v[8 * q + e] = g / (1.f + expf(-g)) * u;
+            // silu(g) u with the SFU exponential and a fast reciprocal: a few fp32 ulps,
+            // far below the bf16 rounding of the stored activation; for g below ~-88 the
+            // reciprocal of an infinite 1 + e^-g gives 0
+            v[8 * q + e] = g * __fdividef(1.f, 1.f + __expf(-g)) * u;
           }
         }
         store_row32(p.y + static_cast<size_t>(row) * p.ldy + col0, v, valid);
@@ -403,10 +408,16 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t m0, uint32_t m1, uint64_t s
   return pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // Dequantise one stage: the thread's codes -> bf16 [256][64] in the 128-byte swizzled K-major
 // layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).  Thread t of the 256 dequant
-// threads handles k-chunk (t & 3) (16 codes, one group) of rows t/4 + 64 i.
-__device__ __forceinline__ void dequant_stage(uint8_t* sb, const DqStage& d, int t) {
+// threads handles k-chunk (t & 3) (16 codes, one group) of rows t/4 + 64 i.  Each 16-byte chunk
+// goes out as one 128-bit shared store: a quarter warp (two rows, eight chunks) then covers all
+// 32 banks once.
+__device__ __forceinline__ void dequant_stage(uint32_t sb, const DqStage& d, int t) {
   const int kc = t & 3;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -426,10 +437,10 @@ __device__ __forceinline__ void dequant_stage(uint8_t* sb, const DqStage& d, int
         o[2 * w + h] = dq_pair(m0, m1, sc2, qb2);
       }
     }
-    uint8_t* rowp = sb + n * 128;
+    const uint32_t rowp = sb + n * 128;
     const int c0 = 2 * kc, c1 = 2 * kc + 1;
-    *reinterpret_cast<int4*>(rowp + ((c0 ^ (n & 7)) << 4)) = make_int4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<int4*>(rowp + ((c1 ^ (n & 7)) << 4)) = make_int4(o[4], o[5], o[6], o[7]);
+    st_shared_v4(rowp + ((c0 ^ (n & 7)) << 4), o[0], o[1], o[2], o[3]);
+    st_shared_v4(rowp + ((c1 ^ (n & 7)) << 4), o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
         ok = false;
         return;
       }
-      dequant_stage(sB(s), d, t);
+      dequant_stage(smem_u32(sB(s)), d, t);
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ready + 8 * s);
