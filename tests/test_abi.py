@@ -176,3 +176,22 @@ def test_qknorm_rope_entry_points_refuse_misaligned_pointers(h3mod):
             h3mod.H3_EINVAL
         assert L.h3_qknorm_rope(ctypes.byref(dd), al, al, None, None, al, al, al, ld, n, ws, 1 << 20, None) == \
             h3mod.H3_EINVAL
+
+
+def test_modcache_build_refuses_misaligned_inputs(h3mod):
+    """The table build reads the embedding by TMA (16-byte aligned rows) and the weights by TMA
+    (16-byte aligned base): a misaligned embedding, weight or bias pointer, or an embedding
+    width that is not a multiple of 8, is refused on the host."""
+    L = h3mod.lib()
+    d = _tiny_dims(h3mod)
+    al, odd = 0x40000, 0x40000 + 4
+    W = (ctypes.c_void_p * 2)(al, al)
+    B = (ctypes.c_void_p * 2)(al, al)
+    # valid arguments up to the launch would reach CUDA; every case below must stop before it
+    assert L.h3_modcache_build(ctypes.byref(d), odd, 77, 96, W, B, 2, al, None) == h3mod.H3_EINVAL
+    assert L.h3_modcache_build(ctypes.byref(d), al, 77, 92, W, B, 2, al, None) == h3mod.H3_EINVAL
+    Wbad = (ctypes.c_void_p * 2)(al, odd)
+    assert L.h3_modcache_build(ctypes.byref(d), al, 77, 96, Wbad, B, 2, al, None) == h3mod.H3_EINVAL
+    Bbad = (ctypes.c_void_p * 2)(al, al + 1)
+    assert L.h3_modcache_build(ctypes.byref(d), al, 77, 96, W, Bbad, 2, al, None) == h3mod.H3_EINVAL
+    assert L.h3_final_modcache_build(ctypes.byref(d), odd, 77, 96, al, al, al, None) == h3mod.H3_EINVAL
