@@ -122,18 +122,31 @@ __device__ __forceinline__ void load8(const bf16* p, float* f) {
   }
 }
 
-__device__ __forceinline__ void store_row32(bf16* dst, const float* v, int valid) {
-  if (valid >= 32) {
+// CW consecutive values of a row: 16-byte stores when the chunk is whole, element stores at the
+// ragged end of the row
+template <int CW>
+__device__ __forceinline__ void store_row(bf16* dst, const float* v, int valid) {
+  if (valid >= CW) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < CW / 8; ++c) {
       const int4 o = make_int4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
                                pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
       reinterpret_cast<int4*>(dst)[c] = o;
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < CW; ++i)
       if (i < valid) dst[i] = f2bf(v[i]);
+  }
+}
+
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CW]) {
+  if constexpr (CW == 32) {
+    tmem_ld32(taddr, r);
+  } else {
+    static_assert(CW == 16, "16- or 32-column chunks");
+    tmem_ld16(taddr, r);
   }
 }
 
@@ -269,27 +282,29 @@ __device__ __forceinline__ void qkv_epilogue(const GemmParams& p, uint32_t tacc,
   }
 }
 
-// Epilogue of one tile for the calling thread's row (TMEM lane = row within the tile).
-template <int EPI>
+// Epilogue of one tile for the calling thread's row (TMEM lane = row within the tile), CW
+// accumulator columns at a time (16 in the INT8 kernels, whose 22 warps leave 80 registers a
+// thread; 32 otherwise).
+template <int EPI, int CW>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc, int row, int nb) {
   const bool row_ok = row < p.M;
   if (EPI == kEpiQkv) {
     qkv_epilogue(p, tacc, row, nb);
   } else if (EPI == kEpiSwiglu) {
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t rg[32], rv[32];
-      tmem_ld32(tacc + c * 32, rg);
-      tmem_ld32(tacc + 128 + c * 32, rv);
+    for (int c = 0; c < 128 / CW; ++c) {
+      uint32_t rg[CW], rv[CW];
+      tmem_ld_cols<CW>(tacc + c * CW, rg);
+      tmem_ld_cols<CW>(tacc + 128 + c * CW, rv);
       tmem_wait_ld();
-      const int col0 = nb * 128 + c * 32;
+      const int col0 = nb * 128 + c * CW;
       if (row_ok && col0 < p.n_y) {
-        float v[32];
-        const int valid = min(32, p.n_y - col0);
+        float v[CW];
+        const int valid = min(CW, p.n_y - col0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < CW / 8; ++q) {
           float bg[8], bv[8];
-          if (p.bias && valid >= 32) {
+          if (p.bias && valid >= CW) {
             load8(p.bias + col0 + 8 * q, bg);
             load8(p.bias + p.n_y + col0 + 8 * q, bv);
           } else {
@@ -310,7 +325,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
             v[8 * q + e] = g * __fdividef(1.f, 1.f + __expf(-g)) * u;
           }
         }
-        store_row32(p.y + static_cast<size_t>(row) * p.ldy + col0, v, valid);
+        store_row<CW>(p.y + static_cast<size_t>(row) * p.ldy + col0, v, valid);
       }
     }
   } else {
@@ -321,18 +336,18 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
                  static_cast<long long>(6 * t.tag[row] + p.m_gate) * p.n_y;
     }
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tacc + c * 32, r);
+    for (int c = 0; c < 256 / CW; ++c) {
+      uint32_t r[CW];
+      tmem_ld_cols<CW>(tacc + c * CW, r);
       tmem_wait_ld();
-      const int col0 = nb * 256 + c * 32;
+      const int col0 = nb * 256 + c * CW;
       if (row_ok && col0 < p.n_y) {
-        const int valid = min(32, p.n_y - col0);
-        float v[32];
+        const int valid = min(CW, p.n_y - col0);
+        float v[CW];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < CW / 8; ++q) {
           float b[8], rs[8], g[8];
-          if (valid >= 32) {
+          if (valid >= CW) {
             if (p.bias) load8(p.bias + col0 + 8 * q, b);
             else {
 #pragma unroll
@@ -360,7 +375,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
             v[8 * q + e] = (EPI == kEpiGateRes) ? rs[e] + g[e] * a : a;
           }
         }
-        store_row32(p.y + static_cast<size_t>(row) * p.ldy + col0, v, valid);
+        store_row<CW>(p.y + static_cast<size_t>(row) * p.ldy + col0, v, valid);
       }
     }
   }
@@ -584,7 +599,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
 #pragma unroll 1
       for (int a = 0; a < C::MSUB; ++a) {
         const int row = mb * C::BM + a * 128 + quad * 32 + lane;
-        gemm_epilogue<EPI>(p, tmem_base + (acc * C::MSUB + a) * G_BN + ((quad * 32) << 16), row, nb);
+        gemm_epilogue<EPI, INT8 ? 16 : 32>(p, tmem_base + (acc * C::MSUB + a) * G_BN + ((quad * 32) << 16), row, nb);
       }
       tc_fence_before();
       __syncwarp();
