@@ -19,7 +19,10 @@ section it follows.  Sources:
   fc2(silu(gate)*value)), "Performance" (dense full attention, linear share of the work).
 - "H3-metal" README (antirez/h3.c): "Checkpoint layout and media pipeline" (fused
   QK-normalisation + RoPE on the interleaved qkv), "Exact DiT fusions".
-- "mlx-h3" README: "Local model layout" (weight-only INT8 group 32, a8g32).
+- "mlx-h3" README: "Local model layout" (weight-only INT8 group 32, a8g32); "Why mlx-h3"
+  (the sampler: 20 schedule steps of the second-order res_multistep solver, which the page
+  names without defining; res_multistep_coefficients follows the published refined
+  exponential solver of Zhang, Song and Chen, 2023, in its multistep form).
 
 Readings where the pages are silent (each also listed in the design notes):
 - the 18 in 18*H is 3 modality tags x 6 modulation tensors, tag-major, tensor order
@@ -30,6 +33,9 @@ Readings where the pages are silent (each also listed in the design notes):
   hd/2 pairs split into contiguous (t, h, w) sections of hd/8, 3hd/16, 3hd/16 pairs;
 - attention is unmasked softmax(q k^T / sqrt(hd)) v over every row;
 - linears carry biases; no nonlinearity is applied to temb inside the library.
+- res_multistep: data prediction D = z - sigma v, log-noise time t = -ln(sigma), D linear in t
+  through the current and previous predictions; first step first-order, a step to sigma 0
+  returns D.
 
 Parity status: the whole block and trunk are "parity unpinned" against the real model (the
 pages print no worked example and no weights are available); each step is pinned separately
@@ -453,13 +459,67 @@ def euler_step(z, v, sigma_now: float, sigma_next: float) -> np.ndarray:
     return np.asarray(z, dtype=np.float64) + (float(sigma_next) - float(sigma_now)) * np.asarray(v, dtype=np.float64)
 
 
-def denoise_step(text_x, z_cond, z_audio, z_video, io, block_weight_list, table_bf16, table_f, tag, tidx, pos, dims,
-                 dsigma_video: float, dsigma_audio: float):
-    """One sampler transition over the packed sequence [text | cond | audio | video]
-    (minimax-h3-mlx README, "Architecture" and "Layout"; mlx-h3 README, "Generate": video and
-    audio advance on their own sigma grids): the entry projections write the latent rows into
-    the hidden stream (stored as bf16, as the stream is), the trunk runs, the output heads give
-    each modality's velocity and the Euler step moves its latents.  Returns (z_audio, z_video).
+def data_prediction(z, v, sigma: float) -> np.ndarray:
+    """The clean-latent estimate behind a rectified-flow velocity: z_sigma = (1 - sigma) x0 +
+    sigma eps and v = eps - x0 give x0 = z - sigma v."""
+    return np.asarray(z, dtype=np.float64) - float(sigma) * np.asarray(v, dtype=np.float64)
+
+
+def res_multistep_coefficients(sigma_prev, sigma: float, sigma_next: float) -> tuple:
+    """Weights (a, c_now, c_prev) of one step z_next = a z + c_now D_now + c_prev D_prev of the
+    second-order multistep exponential integrator that the mlx-h3 README ("Why mlx-h3") names as
+    the sampler (res_multistep).  The pages name the solver but do not define it; this follows
+    the published method it is named for: the refined exponential solver (RES) of Zhang, Song
+    and Chen, "Improved Order Analysis and Design of Exponential Integrator for Diffusion
+    Models Sampling" (2023), in its multistep form.
+
+    Derivation.  With the data prediction D(z, sigma) = z - sigma v, the sampling ODE
+    dz/dsigma = v reads dz/dsigma = (z - D)/sigma; in log-noise time t = -ln(sigma) it is
+    dz/dt = D - z, so over one step of length h = t_next - t = ln(sigma / sigma_next),
+        z(t + h) = e^-h z(t) + integral_0^h e^-(h - u) D(t + u) du.
+    D is taken linear in u through D_now (u = 0) and D_prev (u = r h, r = (t_prev - t) / h < 0),
+    and the two integrals are h phi1(-h) and h^2 phi2(-h) with phi1(x) = (e^x - 1)/x and
+    phi2(x) = (phi1(x) - 1)/x, which gives
+        a = e^-h = sigma_next / sigma,
+        c_now = h (phi1 - phi2 / r),  c_prev = h phi2 / r.
+    Without a previous prediction (sigma_prev None: the first step) D is taken constant: the
+    first-order step a = sigma_next / sigma, c_now = 1 - a, which equals the Euler step
+    z + (sigma_next - sigma) v.  A step to sigma_next = 0 returns D_now (a = 0, c_now = 1), the
+    limit of both forms and the Euler step to zero.  float64 throughout."""
+    sigma = float(sigma)
+    sigma_next = float(sigma_next)
+    if not sigma > 0.0:
+        raise ValueError("sigma must be positive")
+    if sigma_next == 0.0:
+        return 0.0, 1.0, 0.0
+    a = sigma_next / sigma
+    if sigma_prev is None:
+        return a, 1.0 - a, 0.0
+    h = math.log(sigma / sigma_next)
+    r = math.log(sigma / float(sigma_prev)) / h
+    phi1 = -math.expm1(-h) / h
+    phi2 = (1.0 - phi1) / h
+    return a, h * (phi1 - phi2 / r), h * phi2 / r
+
+
+def res_multistep_step(z, v, sigma_prev, sigma: float, sigma_next: float, d_prev=None):
+    """One res_multistep transition of a modality's latents (coefficients above).  Returns
+    (z_next, D_now); D_now is the d_prev of the next step.  d_prev is needed unless sigma_prev
+    is None."""
+    d_now = data_prediction(z, v, sigma)
+    a, c_now, c_prev = res_multistep_coefficients(sigma_prev, sigma, sigma_next)
+    z_next = a * np.asarray(z, dtype=np.float64) + c_now * d_now
+    if c_prev != 0.0:
+        z_next = z_next + c_prev * np.asarray(d_prev, dtype=np.float64)
+    return z_next, d_now
+
+
+def denoise_velocities(text_x, z_cond, z_audio, z_video, io, block_weight_list, table_bf16, table_f, tag, tidx, pos,
+                       dims):
+    """The model evaluation of one sampler transition over the packed sequence [text | cond |
+    audio | video] (minimax-h3-mlx README, "Architecture" and "Layout"): the entry projections
+    write the latent rows into the hidden stream (stored as bf16, as the stream is), the trunk
+    runs, and the output heads give each modality's velocity.  Returns (v_audio, v_video).
     io: synth.io_weights() layout; text_x: the projected text rows (bf16 values)."""
     H = dims.hidden
     parts = [np.asarray(text_x, dtype=np.float64)]
@@ -472,14 +532,36 @@ def denoise_step(text_x, z_cond, z_audio, z_video, io, block_weight_list, table_
     a0 = len(text_x) + len(z_cond)
     v0 = a0 + len(z_audio)
     out = []
-    for r0, z, w, b, ds in ((a0, z_audio, io["head_a"], io["head_a_b"], dsigma_audio),
-                            (v0, z_video, io["head_v"], io["head_v_b"], dsigma_video)):
-        rows = slice(r0, r0 + len(z))
+    for r0, n, w, b in ((a0, len(z_audio), io["head_a"], io["head_a_b"]), (v0, len(z_video), io["head_v"], io["head_v_b"])):
+        rows = slice(r0, r0 + n)
         shift = final_modulation(table_f, tag[rows], tidx[rows], 0, H)
         scale = final_modulation(table_f, tag[rows], tidx[rows], 1, H)
-        v = head_forward(x[rows], shift, scale, w, b, dims.ln_eps)
-        out.append(euler_step(z, v, 0.0, ds))
+        out.append(head_forward(x[rows], shift, scale, w, b, dims.ln_eps))
     return out[0], out[1]
+
+
+def denoise_step(text_x, z_cond, z_audio, z_video, io, block_weight_list, table_bf16, table_f, tag, tidx, pos, dims,
+                 dsigma_video: float, dsigma_audio: float):
+    """One Euler sampler transition (minimax-h3-mlx README, "Layout"; mlx-h3 README,
+    "Generate": video and audio advance on their own sigma grids): the velocities of
+    denoise_velocities move each modality's latents by its own dsigma.  Returns
+    (z_audio, z_video)."""
+    v_a, v_v = denoise_velocities(text_x, z_cond, z_audio, z_video, io, block_weight_list, table_bf16, table_f, tag,
+                                  tidx, pos, dims)
+    return euler_step(z_audio, v_a, 0.0, dsigma_audio), euler_step(z_video, v_v, 0.0, dsigma_video)
+
+
+def denoise_step_multistep(text_x, z_cond, z_audio, z_video, io, block_weight_list, table_bf16, table_f, tag, tidx,
+                           pos, dims, sig_video, sig_audio, d_prev_video=None, d_prev_audio=None):
+    """One res_multistep sampler transition (mlx-h3 README, "Why mlx-h3"): the velocities of
+    denoise_velocities, then res_multistep_step per modality on its own grid.  sig_video,
+    sig_audio: (sigma_prev or None, sigma, sigma_next).  Returns (z_audio, z_video, D_audio,
+    D_video), the D's being the next step's d_prev."""
+    v_a, v_v = denoise_velocities(text_x, z_cond, z_audio, z_video, io, block_weight_list, table_bf16, table_f, tag,
+                                  tidx, pos, dims)
+    za, da = res_multistep_step(z_audio, v_a, *sig_audio, d_prev=d_prev_audio)
+    zv, dv = res_multistep_step(z_video, v_v, *sig_video, d_prev=d_prev_video)
+    return za, zv, da, dv
 
 
 # ----------------------------------------------------------------------------------------
