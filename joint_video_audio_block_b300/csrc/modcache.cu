@@ -217,7 +217,9 @@ __global__ void __launch_bounds__(MC_THREADS, 1) modcache_tc_kernel(const __grid
     }
   } else if (warp < 6) {
     // epilogue: this warp's 32 TMEM lanes are 32 weight rows of each 128-row half; columns are
-    // timesteps t0 + c in three groups (W.hi, W.mid, W.lo)
+    // timesteps t0 + c in three groups (W.hi, W.mid, W.lo).  A half is read out of TMEM and
+    // rounded to bf16 in registers, released to the MMA issuer, and only then stored, so the
+    // next tile's MMAs wait for the TMEM reads alone, not for the table stores.
     const int quad = warp & 3;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, aph ^= 1) {
@@ -229,27 +231,41 @@ __global__ void __launch_bounds__(MC_THREADS, 1) modcache_tc_kernel(const __grid
         const int j = rt * MC_BM + h * 128 + quad * 32 + lane;
         const bool row_ok = j < p.n_out;
         const float bj = (row_ok && p.bias[blk]) ? bf2f(p.bias[blk][j]) : 0.f;
-        bf16* dst = p.table + static_cast<long long>(blk) * p.n_out + j;
         const uint32_t t_acc = tmem + h * MC_ACC_COLS + (static_cast<uint32_t>(quad * 32) << 16);
-#pragma unroll 1
-        for (int c = 0; c < N / 16; ++c) {
-          uint32_t rh[16], rm[16], rl[16];
-          tmem_ld16(t_acc + c * 16, rh);
-          tmem_ld16(t_acc + N + c * 16, rm);
-          tmem_ld16(t_acc + 2 * N + c * 16, rl);
-          tmem_wait_ld();
-          if (row_ok) {
+        uint32_t out[MC_NMAX / 2];  // bf16 pairs (t, t + 1) of this row
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int t = p.t0 + c * 16 + e;
-              const float v = (__uint_as_float(rh[e]) + __uint_as_float(rm[e])) + __uint_as_float(rl[e]);
-              if (t < p.T) dst[static_cast<long long>(t) * p.t_stride] = f2bf(v + bj);
+        for (int c = 0; c < MC_NMAX / 16; ++c) {
+          if (c < N / 16) {
+            uint32_t rh[16], rm[16], rl[16];
+            tmem_ld16(t_acc + c * 16, rh);
+            tmem_ld16(t_acc + N + c * 16, rm);
+            tmem_ld16(t_acc + 2 * N + c * 16, rl);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float v0 = (__uint_as_float(rh[e]) + __uint_as_float(rm[e])) + __uint_as_float(rl[e]);
+              const float v1 = (__uint_as_float(rh[e + 1]) + __uint_as_float(rm[e + 1])) + __uint_as_float(rl[e + 1]);
+              out[c * 8 + e / 2] = pack_bf16x2(v0 + bj, v1 + bj);
             }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_accempty + 8 * h);
+        if (row_ok) {
+          bf16* dst = p.table + static_cast<long long>(blk) * p.n_out + j;
+#pragma unroll
+          for (int c = 0; c < MC_NMAX / 16; ++c)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int t = p.t0 + c * 16 + e;
+              if (c < N / 16 && t < p.T) {
+                const uint32_t pr = out[c * 8 + e / 2];
+                dst[static_cast<long long>(t) * p.t_stride] =
+                    __ushort_as_bfloat16(static_cast<unsigned short>((e & 1) ? (pr >> 16) : (pr & 0xffffu)));
+              }
+            }
+        }
       }
     }
   } else {
