@@ -153,6 +153,35 @@ h3_status h3_head_forward(const h3_dims* dims, const void* x_rows, int n_rows, c
                           const void* table_f, long long t_stride, const float* w, const float* b, int K_out,
                           float* v_out, float* z_inout, float dsigma, void* stream);
 
+/* ---- the second-order sampler (mlx-h3 README, "Why mlx-h3": 20 schedule steps of the
+ * res_multistep solver).  The page names the solver without defining it; this is the multistep
+ * form of the refined exponential solver (Zhang, Song and Chen, "Improved Order Analysis and
+ * Design of Exponential Integrator for Diffusion Models Sampling", 2023).  With the data
+ * prediction D = z - sigma v of a rectified-flow velocity v, one step is
+ *   z_next = a z + c_now D + c_prev D_prev,
+ * D_prev being the previous step's prediction of the same modality. ---- */
+typedef struct {
+  float sigma;   /* the noise level the velocity is evaluated at (> 0) */
+  float a, c_now, c_prev;
+} h3_ms_step;
+
+/* HOST: the weights of one res_multistep step from sigma to sigma_next (0 <= sigma_next <
+ * sigma), sigma_prev being the previous step's sigma (> sigma), or <= 0 for the first step,
+ * which is then first order (c_prev = 0; the Euler step).  A step to sigma_next = 0 returns D
+ * (a = 0, c_now = 1).  Computed in double precision, rounded once to float.  Anything else
+ * returns H3_EINVAL. */
+h3_status h3_res_multistep_step(float sigma_prev, float sigma, float sigma_next, h3_ms_step* out);
+
+/* h3_head_forward with a res_multistep update instead of the Euler one: v as there, then per
+ * element D = z - step->sigma * v, z = a z + c_now D + c_prev d_prev, d_prev = D (float32).
+ * step: HOST; z_inout, d_prev_inout: device f32 [n_rows, K_out], both required; d_prev_inout is
+ * read only when step->c_prev != 0 (it may hold anything on the first step) and always
+ * written.  v_out: device f32 [n_rows, K_out] or NULL. */
+h3_status h3_head_forward_ms(const h3_dims* dims, const void* x_rows, int n_rows, const uint8_t* tag,
+                             const int32_t* tidx, const void* table_f, long long t_stride, const float* w,
+                             const float* b, int K_out, const h3_ms_step* step, float* v_out, float* z_inout,
+                             float* d_prev_inout, void* stream);
+
 /* HOST: the sampling grid of one schedule, steps + 1 values from 1 to 0: a float32 linspace
  * (float32 step; first half start + step*i, second half end - step*(n-1-i), each one fused
  * multiply-add) followed by the time shift s sigma / (1 + (s - 1) sigma) in float32.
@@ -184,6 +213,18 @@ h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_b
                           float* z_video, float* z_audio, void* x, const uint8_t* tag, const int32_t* tidx,
                           const float* pos, float dsigma_video, float dsigma_audio, void* workspace, size_t ws_bytes,
                           unsigned flags, void* stream);
+
+/* h3_denoise_step with res_multistep updates: the same entry, trunk and heads, then each
+ * modality's latents take the step of h3_head_forward_ms with its own weights (step_video,
+ * step_audio: HOST, from h3_res_multistep_step on the modality's grid) and its own previous
+ * prediction (d_prev_video: device f32 [video_rows, k_video], d_prev_audio: [audio_rows,
+ * k_audio]; read when c_prev != 0, always overwritten with this step's prediction). */
+h3_status h3_denoise_step_ms(const h3_dims* dims, const h3_block_w* blocks, int n_blocks, const void* table,
+                             const void* table_f, int T, const h3_io_w* io, const void* text_x, const float* z_cond,
+                             float* z_video, float* z_audio, float* d_prev_video, float* d_prev_audio, void* x,
+                             const uint8_t* tag, const int32_t* tidx, const float* pos, const h3_ms_step* step_video,
+                             const h3_ms_step* step_audio, void* workspace, size_t ws_bytes, unsigned flags,
+                             void* stream);
 
 /* ---- step entry points (each row of the block on its own; used for per-step parity) ---- */
 

@@ -455,11 +455,16 @@ h3_status h3_trunk_forward(const h3_dims* dims, const h3_block_w* blocks, int n_
   return H3_OK;
 }
 
-h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_blocks, const void* table,
-                          const void* table_f, int T, const h3_io_w* io, const void* text_x, const float* z_cond,
-                          float* z_video, float* z_audio, void* x, const uint8_t* tag, const int32_t* tidx,
-                          const float* pos, float dsigma_video, float dsigma_audio, void* workspace, size_t ws_bytes,
-                          unsigned flags, void* stream) {
+}  // extern "C"
+
+namespace {
+// The model evaluation shared by both sampler transitions: the latent rows enter the hidden
+// stream through their patch projections (text rows are copied in), then the trunk runs.
+h3_status denoise_entry_trunk(const h3_dims* dims, const h3_block_w* blocks, int n_blocks, const void* table,
+                              const void* table_f, int T, const h3_io_w* io, const void* text_x, const float* z_cond,
+                              const float* z_video, const float* z_audio, void* x, const uint8_t* tag,
+                              const int32_t* tidx, const float* pos, void* workspace, size_t ws_bytes, unsigned flags,
+                              void* stream) {
   if (!dims_ok(dims) || !io || !x || !table_f || !tag || !tidx) return H3_EINVAL;
   const int H = dims->hidden;
   const int L = io->text_rows, C = io->cond_rows, A = io->audio_rows, V = io->video_rows;
@@ -469,9 +474,7 @@ h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_b
   const size_t row_bytes = static_cast<size_t>(H) * 2;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* xb = static_cast<char*>(x);
-  const long long tf_stride = 6LL * H;
   h3_status s = H3_OK;
-  // entry
   if (L && cudaMemcpyAsync(xb, text_x, L * row_bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess) return H3_ECUDA;
   if (C && (s = h3_embed_rows(dims, z_cond, io->k_video, io->patch_v, io->patch_v_b, C, xb + L * row_bytes, stream)))
     return s;
@@ -481,10 +484,24 @@ h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_b
   if (V && (s = h3_embed_rows(dims, z_video, io->k_video, io->patch_v, io->patch_v_b, V,
                               xb + static_cast<size_t>(L + C + A) * row_bytes, stream)))
     return s;
-  // trunk
-  if ((s = h3_trunk_forward(dims, blocks, n_blocks, table, T, x, n, tag, tidx, pos, workspace, ws_bytes, flags,
-                            stream)))
-    return s;
+  return h3_trunk_forward(dims, blocks, n_blocks, table, T, x, n, tag, tidx, pos, workspace, ws_bytes, flags, stream);
+}
+}  // namespace
+
+extern "C" {
+
+h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_blocks, const void* table,
+                          const void* table_f, int T, const h3_io_w* io, const void* text_x, const float* z_cond,
+                          float* z_video, float* z_audio, void* x, const uint8_t* tag, const int32_t* tidx,
+                          const float* pos, float dsigma_video, float dsigma_audio, void* workspace, size_t ws_bytes,
+                          unsigned flags, void* stream) {
+  h3_status s = denoise_entry_trunk(dims, blocks, n_blocks, table, table_f, T, io, text_x, z_cond, z_video, z_audio,
+                                    x, tag, tidx, pos, workspace, ws_bytes, flags, stream);
+  if (s) return s;
+  const int L = io->text_rows, C = io->cond_rows, A = io->audio_rows, V = io->video_rows;
+  const size_t row_bytes = static_cast<size_t>(dims->hidden) * 2;
+  char* xb = static_cast<char*>(x);
+  const long long tf_stride = 6LL * dims->hidden;
   // exit + Euler transition
   if (A && (s = h3_head_forward(dims, xb + static_cast<size_t>(L + C) * row_bytes, A, tag + (L + C), tidx + (L + C),
                                 table_f, tf_stride, io->head_a, io->head_a_b, io->k_audio, nullptr, z_audio,
@@ -493,6 +510,33 @@ h3_status h3_denoise_step(const h3_dims* dims, const h3_block_w* blocks, int n_b
   if (V && (s = h3_head_forward(dims, xb + static_cast<size_t>(L + C + A) * row_bytes, V, tag + (L + C + A),
                                 tidx + (L + C + A), table_f, tf_stride, io->head_v, io->head_v_b, io->k_video,
                                 nullptr, z_video, dsigma_video, stream)))
+    return s;
+  return H3_OK;
+}
+
+h3_status h3_denoise_step_ms(const h3_dims* dims, const h3_block_w* blocks, int n_blocks, const void* table,
+                             const void* table_f, int T, const h3_io_w* io, const void* text_x, const float* z_cond,
+                             float* z_video, float* z_audio, float* d_prev_video, float* d_prev_audio, void* x,
+                             const uint8_t* tag, const int32_t* tidx, const float* pos, const h3_ms_step* step_video,
+                             const h3_ms_step* step_audio, void* workspace, size_t ws_bytes, unsigned flags,
+                             void* stream) {
+  if (!io || !step_video || !step_audio || (io->audio_rows && !d_prev_audio) || (io->video_rows && !d_prev_video))
+    return H3_EINVAL;
+  h3_status s = denoise_entry_trunk(dims, blocks, n_blocks, table, table_f, T, io, text_x, z_cond, z_video, z_audio,
+                                    x, tag, tidx, pos, workspace, ws_bytes, flags, stream);
+  if (s) return s;
+  const int L = io->text_rows, C = io->cond_rows, A = io->audio_rows, V = io->video_rows;
+  const size_t row_bytes = static_cast<size_t>(dims->hidden) * 2;
+  char* xb = static_cast<char*>(x);
+  const long long tf_stride = 6LL * dims->hidden;
+  // exit + res_multistep transition
+  if (A && (s = h3_head_forward_ms(dims, xb + static_cast<size_t>(L + C) * row_bytes, A, tag + (L + C),
+                                   tidx + (L + C), table_f, tf_stride, io->head_a, io->head_a_b, io->k_audio,
+                                   step_audio, nullptr, z_audio, d_prev_audio, stream)))
+    return s;
+  if (V && (s = h3_head_forward_ms(dims, xb + static_cast<size_t>(L + C + A) * row_bytes, V, tag + (L + C + A),
+                                   tidx + (L + C + A), table_f, tf_stride, io->head_v, io->head_v_b, io->k_video,
+                                   step_video, nullptr, z_video, d_prev_video, stream)))
     return s;
   return H3_OK;
 }

@@ -1,4 +1,4 @@
-// Trunk entry and exit, and the sampler's Euler transition.
+// Trunk entry and exit, and the sampler's transitions (Euler and second-order res_multistep).
 //
 // "minimax-h3-mlx" README, "Architecture": modality-specific behaviour comes only from the two
 // input patch projections, the per-row AdaLN tag and the two output heads; "Porting notes":
@@ -13,8 +13,13 @@
 //   head_kernel    v[r] = W (LN(x[r]) (1 + scale) + shift) + b for one modality's rows, the
 //                  final AdaLN gathered per row from a [T][3 tags][2][H] table; float32
 //                  weights [K_out, H] (K_out <= 128) and float32 arithmetic throughout;
-//                  optionally also the Euler transition z[r] += dsigma * v[r] on the float32
-//                  latent rows.
+//                  optionally also the sampler update of the float32 latent rows: the Euler
+//                  transition z[r] += dsigma * v[r], or a res_multistep step (mlx-h3 README,
+//                  "Why mlx-h3": the sampler's second-order solver; the page names it without
+//                  defining it, and the step here is the multistep form of the refined
+//                  exponential solver of Zhang, Song and Chen, 2023): with the data prediction
+//                  D = z - sigma v, z <- a z + c_now D + c_prev D_prev, D_prev <- D, the weights
+//                  from h3_res_multistep_step.
 #include <cmath>
 
 #include "../../include/h3.h"
@@ -101,8 +106,11 @@ struct HeadArgs {
   int K_out;
   float eps;
   float* v;  // [n_rows, K_out] or null
-  float* z;  // [n_rows, K_out] or null: z += dsigma * v
+  float* z;  // [n_rows, K_out] or null: the sampler update of the latent rows
   float dsigma;
+  int ms;           // 0: Euler, z += dsigma v; 1: res_multistep
+  float sigma, ca, cn, cp;  // res_multistep: D = z - sigma v, z <- ca z + cn D + cp D_prev
+  float* dprev;     // res_multistep: [n_rows, K_out], read when cp != 0, then overwritten with D
 };
 
 __global__ void __launch_bounds__(256) head_kernel(const HeadArgs a) {
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(256) head_kernel(const HeadArgs a) {
         for (int j = 0; j < HD_NJ; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
   }
-  // 3. bias, optional v, optional Euler update of the latent rows
+  // 3. bias, optional v, optional sampler update of the latent rows
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = r0 + ty * 4 + i;
@@ -201,7 +209,18 @@ __global__ void __launch_bounds__(256) head_kernel(const HeadArgs a) {
       const float v = acc[i][j] + (a.b ? a.b[o] : 0.f);
       const size_t idx = static_cast<size_t>(r) * a.K_out + o;
       if (a.v) a.v[idx] = v;
-      if (a.z) a.z[idx] = fmaf(a.dsigma, v, a.z[idx]);
+      if (a.z) {
+        const float z = a.z[idx];
+        if (a.ms) {
+          const float dn = fmaf(-a.sigma, v, z);
+          float zn = fmaf(a.cn, dn, a.ca * z);
+          if (a.cp != 0.f) zn = fmaf(a.cp, a.dprev[idx], zn);
+          a.z[idx] = zn;
+          a.dprev[idx] = dn;
+        } else {
+          a.z[idx] = fmaf(a.dsigma, v, z);
+        }
+      }
     }
   }
 }
@@ -225,20 +244,71 @@ extern "C" h3_status h3_embed_rows(const h3_dims* dims, const float* z, int K, c
   return cudaGetLastError() == cudaSuccess ? H3_OK : H3_ECUDA;
 }
 
-extern "C" h3_status h3_head_forward(const h3_dims* dims, const void* x_rows, int n_rows, const uint8_t* tag,
-                                     const int32_t* tidx, const void* table_f, long long t_stride, const float* w,
-                                     const float* b, int K_out, float* v_out, float* z_inout, float dsigma,
-                                     void* stream) {
+namespace {
+h3_status launch_head(const h3_dims* dims, const void* x_rows, int n_rows, const uint8_t* tag, const int32_t* tidx,
+                      const void* table_f, long long t_stride, const float* w, const float* b, int K_out, float* v_out,
+                      float* z_inout, float dsigma, const h3_ms_step* ms, float* d_prev, void* stream) {
   if (!dims || !x_rows || !tag || !tidx || !table_f || !w || K_out <= 0 || K_out > HD_NMAX || n_rows < 0)
     return H3_EINVAL;
   if (!v_out && !z_inout) return H3_EINVAL;
   const int H = dims->hidden;
   if (H <= 0 || H % 64 || !a16(x_rows) || t_stride < 6LL * H) return H3_EINVAL;
+  if (ms && (!z_inout || !d_prev || !(ms->sigma > 0.f))) return H3_EINVAL;
   if (n_rows == 0) return H3_OK;
   HeadArgs a{static_cast<const bf16*>(x_rows), n_rows, H, tag, tidx, static_cast<const bf16*>(table_f), t_stride,
-             w, b, K_out, dims->ln_eps, v_out, z_inout, dsigma};
+             w, b, K_out, dims->ln_eps, v_out, z_inout, dsigma, ms ? 1 : 0, ms ? ms->sigma : 0.f, ms ? ms->a : 0.f,
+             ms ? ms->c_now : 0.f, ms ? ms->c_prev : 0.f, d_prev};
   head_kernel<<<cdiv(n_rows, HD_ROWS), 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? H3_OK : H3_ECUDA;
+}
+}  // namespace
+
+extern "C" h3_status h3_head_forward(const h3_dims* dims, const void* x_rows, int n_rows, const uint8_t* tag,
+                                     const int32_t* tidx, const void* table_f, long long t_stride, const float* w,
+                                     const float* b, int K_out, float* v_out, float* z_inout, float dsigma,
+                                     void* stream) {
+  return launch_head(dims, x_rows, n_rows, tag, tidx, table_f, t_stride, w, b, K_out, v_out, z_inout, dsigma, nullptr,
+                     nullptr, stream);
+}
+
+extern "C" h3_status h3_head_forward_ms(const h3_dims* dims, const void* x_rows, int n_rows, const uint8_t* tag,
+                                        const int32_t* tidx, const void* table_f, long long t_stride, const float* w,
+                                        const float* b, int K_out, const h3_ms_step* step, float* v_out,
+                                        float* z_inout, float* d_prev_inout, void* stream) {
+  if (!step) return H3_EINVAL;
+  return launch_head(dims, x_rows, n_rows, tag, tidx, table_f, t_stride, w, b, K_out, v_out, z_inout, 0.f, step,
+                     d_prev_inout, stream);
+}
+
+// The weights of one res_multistep step, in double precision, rounded once to float.  In
+// log-noise time t = -ln(sigma) the sampling ODE is dz/dt = D - z; over a step of length
+// h = ln(sigma / sigma_next), with D linear in t through D_now and D_prev (at r h,
+// r = ln(sigma / sigma_prev) / h < 0), variation of constants gives
+//   a = e^-h,  c_now = h (phi1 - phi2 / r),  c_prev = h phi2 / r,
+// phi1 = (1 - e^-h) / h and phi2 = (1 - phi1) / h.  The first step (no previous prediction)
+// takes D constant: a = sigma_next / sigma, c_now = 1 - a (the Euler step); a step to 0
+// returns D (a = 0, c_now = 1).
+extern "C" h3_status h3_res_multistep_step(float sigma_prev, float sigma, float sigma_next, h3_ms_step* out) {
+  if (!out || !(sigma > 0.f) || !(sigma_next >= 0.f) || !(sigma_next < sigma)) return H3_EINVAL;
+  const bool first = !(sigma_prev > 0.f);
+  if (!first && !(sigma_prev > sigma)) return H3_EINVAL;
+  const double s = sigma, sn = sigma_next, sp = sigma_prev;
+  double a = 0.0, cn = 1.0, cp = 0.0;
+  if (sn > 0.0) {
+    a = sn / s;
+    cn = 1.0 - a;
+    if (!first) {
+      const double h = std::log(s / sn), r = std::log(s / sp) / h;
+      const double phi1 = -std::expm1(-h) / h, phi2 = (1.0 - phi1) / h;
+      cn = h * (phi1 - phi2 / r);
+      cp = h * phi2 / r;
+    }
+  }
+  out->sigma = sigma;
+  out->a = static_cast<float>(a);
+  out->c_now = static_cast<float>(cn);
+  out->c_prev = static_cast<float>(cp);
+  return H3_OK;
 }
 
 extern "C" h3_status h3_final_modcache_build(const h3_dims* dims, const float* temb, int T, int Dt, const void* w,

@@ -26,6 +26,7 @@ EXPORTS = (
     "h3_status_str", "h3_kernel_timer_start", "h3_kernel_timer_read", "h3_qkv_project",
     "h3_qkv_project_workspace_size", "h3_diag_expire_wait", "h3_attention_sparse", "h3_embed_rows",
     "h3_final_modcache_build", "h3_head_forward", "h3_sigma_schedule", "h3_denoise_step",
+    "h3_res_multistep_step", "h3_head_forward_ms", "h3_denoise_step_ms",
 )
 
 # largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
@@ -62,6 +63,10 @@ class h3_io_w(ctypes.Structure):
                 ("head_a", ctypes.c_void_p), ("head_a_b", ctypes.c_void_p)]
 
 
+class h3_ms_step(ctypes.Structure):
+    _fields_ = [("sigma", ctypes.c_float), ("a", ctypes.c_float), ("c_now", ctypes.c_float), ("c_prev", ctypes.c_float)]
+
+
 _lib = None
 
 
@@ -73,6 +78,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         vp, i32, i64, u32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_uint, ctypes.c_size_t
         D, LW, BW = ctypes.POINTER(h3_dims), ctypes.POINTER(h3_linear), ctypes.POINTER(h3_block_w)
+        MS = ctypes.POINTER(h3_ms_step)
         sig = {
             "h3_workspace_size": (sz, [D, i32]),
             "h3_modcache_build": (i32, [D, vp, i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, vp]),
@@ -92,6 +98,10 @@ def lib():
             "h3_sigma_schedule": (i32, [i32, ctypes.c_float, ctypes.POINTER(ctypes.c_float)]),
             "h3_denoise_step": (i32, [D, BW, i32, vp, vp, i32, ctypes.POINTER(h3_io_w), vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_float, ctypes.c_float, vp, sz, u32, vp]),
+            "h3_res_multistep_step": (i32, [ctypes.c_float, ctypes.c_float, ctypes.c_float, MS]),
+            "h3_head_forward_ms": (i32, [D, vp, i32, vp, vp, vp, i64, vp, vp, i32, MS, vp, vp, vp, vp]),
+            "h3_denoise_step_ms": (i32, [D, BW, i32, vp, vp, i32, ctypes.POINTER(h3_io_w), vp, vp, vp, vp, vp, vp, vp,
+                                         vp, vp, vp, MS, MS, vp, sz, u32, vp]),
             "h3_last_device_error": (i32, [vp, ctypes.POINTER(u32)]),
             "h3_kernel_timer_start": (i32, [i32]),
             "h3_diag_expire_wait": (i32, [u32, vp]),
@@ -227,6 +237,29 @@ def h3_denoise_step(dims, blocks, n_blocks, table, table_f, T, io, text_x, z_con
     _check(lib().h3_denoise_step(ctypes.byref(dims), arr, n_blocks, table, table_f, T, ctypes.byref(io), text_x, z_cond,
                                  z_video, z_audio, x, tag, tidx, pos, dsigma_video, dsigma_audio, workspace, ws_bytes,
                                  flags, stream), "h3_denoise_step")
+
+
+def h3_res_multistep_step(sigma_prev, sigma, sigma_next) -> h3_ms_step:
+    """Host-side weights of one res_multistep step (sigma_prev <= 0 or None: the first step)."""
+    out = h3_ms_step()
+    _check(lib().h3_res_multistep_step(-1.0 if sigma_prev is None else sigma_prev, sigma, sigma_next,
+                                       ctypes.byref(out)), "h3_res_multistep_step")
+    return out
+
+
+def h3_head_forward_ms(dims, x_rows, n_rows, tag, tidx, table_f, t_stride, w, b, K_out, step, v_out, z_inout,
+                       d_prev_inout, stream):
+    _check(lib().h3_head_forward_ms(ctypes.byref(dims), x_rows, n_rows, tag, tidx, table_f, t_stride, w, b, K_out,
+                                    ctypes.byref(step), v_out, z_inout, d_prev_inout, stream), "h3_head_forward_ms")
+
+
+def h3_denoise_step_ms(dims, blocks, n_blocks, table, table_f, T, io, text_x, z_cond, z_video, z_audio, d_prev_video,
+                       d_prev_audio, x, tag, tidx, pos, step_video, step_audio, workspace, ws_bytes, flags, stream):
+    arr = (h3_block_w * n_blocks)(*blocks)
+    _check(lib().h3_denoise_step_ms(ctypes.byref(dims), arr, n_blocks, table, table_f, T, ctypes.byref(io), text_x,
+                                    z_cond, z_video, z_audio, d_prev_video, d_prev_audio, x, tag, tidx, pos,
+                                    ctypes.byref(step_video), ctypes.byref(step_audio), workspace, ws_bytes, flags,
+                                    stream), "h3_denoise_step_ms")
 
 
 def make_io_w(t: dict, text_rows, cond_rows, audio_rows, video_rows, k_video=96, k_audio=32):

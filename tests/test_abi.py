@@ -195,3 +195,47 @@ def test_modcache_build_refuses_misaligned_inputs(h3mod):
     Bbad = (ctypes.c_void_p * 2)(al, al + 1)
     assert L.h3_modcache_build(ctypes.byref(d), al, 77, 96, W, Bbad, 2, al, None) == h3mod.H3_EINVAL
     assert L.h3_final_modcache_build(ctypes.byref(d), odd, 77, 96, al, al, al, None) == h3mod.H3_EINVAL
+
+
+def test_res_multistep_weights_are_the_oracle_s_rounded_to_float(h3mod):
+    """Host-only entry point: the library's res_multistep weights are the oracle's float64
+    weights rounded once to float32, on the grids a run uses (video shift 12, audio shift 3,
+    20 and 40 steps): first step (no previous sigma), interior steps, and the step to 0."""
+    import numpy as np
+
+    import oracle.h3_oracle as O
+
+    for steps, shift in ((20, 12.0), (20, 3.0), (40, 12.0), (40, 3.0)):
+        sig = O.shifted_sigmas(steps, shift).astype(np.float64)
+        for i in range(steps):
+            prev = None if i == 0 else float(sig[i - 1])
+            got = h3mod.h3_res_multistep_step(prev, float(sig[i]), float(sig[i + 1]))
+            want = O.res_multistep_coefficients(prev, float(sig[i]), float(sig[i + 1]))
+            assert got.sigma == np.float32(sig[i])
+            for g, w in zip((got.a, got.c_now, got.c_prev), want):
+                # double-precision weights rounded once: within one float32 ulp of the oracle's
+                assert abs(g - w) <= np.spacing(np.float32(abs(w))) + 1e-12, (steps, shift, i, g, w)
+            if i + 1 == steps:
+                assert (got.a, got.c_now, got.c_prev) == (0.0, 1.0, 0.0)
+            if i == 0:
+                assert got.c_prev == 0.0
+
+
+def test_res_multistep_arguments_refused(h3mod):
+    L = h3mod.lib()
+    out = h3mod.h3_ms_step()
+    f = ctypes.c_float
+    bad = ((0.9, 0.0, 0.0), (0.9, 0.5, 0.5), (0.9, 0.5, 0.6), (0.9, 0.5, -0.1), (0.4, 0.5, 0.25))
+    for sp, s, sn in bad:
+        assert L.h3_res_multistep_step(f(sp), f(s), f(sn), ctypes.byref(out)) == h3mod.H3_EINVAL, (sp, s, sn)
+    assert L.h3_res_multistep_step(f(-1.0), f(0.5), f(0.25), None) == h3mod.H3_EINVAL
+    d = _tiny_dims(h3mod)
+    al = 0x2000
+    step = h3mod.h3_res_multistep_step(None, 0.5, 0.25)
+    # the multistep head needs both the latents and the previous-prediction buffer
+    assert L.h3_head_forward_ms(ctypes.byref(d), al, 8, al, al, al, 6 * 192, al, None, 96, ctypes.byref(step), None,
+                                al, None, None) == h3mod.H3_EINVAL
+    assert L.h3_head_forward_ms(ctypes.byref(d), al, 8, al, al, al, 6 * 192, al, None, 96, ctypes.byref(step), al,
+                                None, al, None) == h3mod.H3_EINVAL
+    assert L.h3_head_forward_ms(ctypes.byref(d), al, 8, al, al, al, 6 * 192, al, None, 96, None, None, al, al,
+                                None) == h3mod.H3_EINVAL
