@@ -7,10 +7,13 @@
 //   warp 0      TMA producer: A tile 128x64 and B tile 256x64 per stage (128-byte swizzle)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128, N=256, K=16 steps)
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bias / SwiGLU / gate+residual, store
-//   warps 6..21 (INT8 only) load the u8 codes of each stage from global memory (three stages
-//               ahead, into registers) and write them dequantised into the swizzled bf16 B tile;
-//               sixteen warps rather than eight hide more of the dequantisation's latency
-//               (measured on the INT8 GEMMs at 12,936 rows: 3 - 10% faster)
+//   warps 6..21 (INT8 only) two groups of eight that take the stages in turn: a warp loads
+//               the u8 codes, scales and qbias of its group's next stage from global memory
+//               into registers right after handing the current stage to the tensor core, and
+//               writes them dequantised into the swizzled bf16 B tile.  With no load in flight
+//               when a warp issues its proxy fence, the fence waits for the shared stores
+//               alone (measured on the INT8 GEMMs at 12,936 rows: 8 - 17% faster than sixteen
+//               warps each keeping three stages of loads in flight across their fences)
 // Two 256-column accumulators in TMEM let the epilogue of tile i overlap the mainloop of i+1.
 //
 // Epilogues ("minimax-h3-mlx" README, "Validation" and "AdaLN: measure, do not reason";
@@ -49,7 +52,7 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * G_BK * 2;
   static constexpr int STAGES = INT8 ? 3 : 4;
   static constexpr int STAGE_BYTES = A_BYTES + G_B_BYTES;
-  static constexpr int THREADS = INT8 ? 192 + 32 * 16 : 192;  // INT8: 16 dequant warps
+  static constexpr int THREADS = INT8 ? 192 + 32 * 16 : 192;  // INT8: 2 groups of 8 dequant warps
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 };
 
@@ -381,12 +384,12 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
   }
 }
 
-// One dequant stage of the calling thread: its two rows' 16-code chunk (k-chunk t & 3 of the
-// stage's 64 k) and the scale and qbias of the group that chunk belongs to.  Loaded from global
-// memory three stages ahead of use, so the loads overlap the dequantisation of earlier stages.
+// One dequant stage of the calling thread: its four rows' 16-code chunk (k-chunk t & 3 of the
+// stage's 64 k) and the scale and qbias of the group that chunk belongs to.
+constexpr int DQ_ROWS = 4;  // rows per dequant thread: 256 threads of a warp group cover 256 rows
 struct DqStage {
-  int4 codes[2];
-  float sc[2], qb[2];
+  int4 codes[DQ_ROWS];
+  float sc[DQ_ROWS], qb[DQ_ROWS];
 };
 
 __device__ __forceinline__ void dq_load_stage(const GemmParams& p, const uint8_t* w, int brow0, int brow1, int kb,
@@ -395,8 +398,8 @@ __device__ __forceinline__ void dq_load_stage(const GemmParams& p, const uint8_t
   const int g = kb * 2 + (kc >> 1);
   const int k0 = kb * 64 + kc * 16;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int n = (t >> 2) + 128 * i;  // row within the 256-row tile
+  for (int i = 0; i < DQ_ROWS; ++i) {
+    const int n = (t >> 2) + 64 * i;  // row within the 256-row tile
     const int grow = (n < 128) ? brow0 + n : brow1 + (n - 128);
     const bool ok = grow < p.w_rows && k0 < p.K;  // K % 32 == 0: a 16-code chunk is all in or all out
     const size_t gi = static_cast<size_t>(grow) * p.groups + g;
@@ -430,15 +433,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // Dequantise one stage: the thread's codes -> bf16 [256][64] in the 128-byte swizzled K-major
-// layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).  Thread t of the 512 dequant
-// threads handles k-chunk (t & 3) (16 codes, one group) of rows t/4 + 128 i.  Each 16-byte chunk
-// goes out as one 128-bit shared store: a quarter warp (two rows, eight chunks) then covers all
-// 32 banks once.
+// layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).  Thread t of the 256 threads of
+// a dequant warp group handles k-chunk (t & 3) (16 codes, one group) of rows t/4 + 64 i.  Each
+// 16-byte chunk goes out as one 128-bit shared store: a quarter warp (two rows, eight chunks)
+// then covers all 32 banks once.
 __device__ __forceinline__ void dequant_stage(uint32_t sb, const DqStage& d, int t) {
   const int kc = t & 3;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int n = (t >> 2) + 128 * i;
+  for (int i = 0; i < DQ_ROWS; ++i) {
+    const int n = (t >> 2) + 64 * i;
     const uint64_t sc2 = (static_cast<uint64_t>(__float_as_uint(d.sc[i])) << 32) | __float_as_uint(d.sc[i]);
     const uint64_t qb2 = (static_cast<uint64_t>(__float_as_uint(d.qb[i])) << 32) | __float_as_uint(d.qb[i]);
     const uint32_t cw[4] = {(uint32_t)d.codes[i].x, (uint32_t)d.codes[i].y, (uint32_t)d.codes[i].z,
@@ -484,7 +487,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_ready + 8 * s, 16);
+      mbar_init(bar_ready + 8 * s, 8);  // the eight warps of the group that dequantises the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
@@ -610,10 +613,14 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       }
     }
   } else if (INT8) {
-    const int t = threadIdx.x - 192;  // 0..511
-    // The CTA's (tile, kb) stage sequence.  A stage's codes, scales and qbias are loaded into
-    // one of three register slots three stages ahead of their use; the loop is unrolled over
-    // the slots so no slot is ever copied (a copy would wait for the loads in flight).
+    // Two groups of eight dequant warps take the CTA's (tile, kb) stages in turn: group g
+    // dequantises stages g, g + 2, g + 4, ...  A warp loads the codes, scales and qbias of its
+    // next stage right after the proxy fence of the current one, into the registers it has just
+    // consumed, and they arrive while the other group works.  So no load is in flight when a
+    // warp issues its fence: the fence that hands a B tile to the tensor core waits for the
+    // warp's shared stores alone.
+    const int grp = (threadIdx.x - 192) >> 8;
+    const int t = (threadIdx.x - 192) & 255;
     struct Cursor {
       int tile, kb, nb;
     };
@@ -638,42 +645,30 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       int mb;
       tile_coords(cur.tile, p.m_tiles, p.n_tiles, p.group_m, mb, cur.nb);
     }
-    Cursor ahead = cur;  // the stage whose scales are loaded next
-    DqStage d0, d1, d2;
-    prefetch(ahead, d0);
-    advance(ahead);
-    prefetch(ahead, d1);
-    advance(ahead);
-    prefetch(ahead, d2);
-    advance(ahead);
-    int s = 0;
-    uint32_t ph = 0;
+    int q = 0;  // stage index in the CTA's sequence: ring slot q % S, phase (q / S) & 1
+    if (grp == 1) {
+      advance(cur);
+      q = 1;
+    }
+    DqStage d;
+    prefetch(cur, d);
     bool ok = true;
-    // one stage: wait until the MMA has released B slot s, dequantise slot d into it, then
-    // refill d three stages ahead
-    auto stage = [&](DqStage& d) {
-      if (!ok || cur.tile >= p.num_tiles) return;
-      if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ec, kErrGemmDequant)) {
+    while (cur.tile < p.num_tiles) {
+      const int s = q % S;
+      if (!mbar_wait(bar_empty + 8 * s, ((q / S) & 1) ^ 1, ec, kErrGemmDequant)) {
         ok = false;
-        return;
+        break;
       }
       dequant_stage(smem_u32(sB(s)), d, t);
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ready + 8 * s);
-      if (++s == S) {
-        s = 0;
-        ph ^= 1;
-      }
-      prefetch(ahead, d);
-      advance(ahead);
       advance(cur);
-    };
-    while (ok && cur.tile < p.num_tiles) {
-      stage(d0);
-      stage(d1);
-      stage(d2);
+      advance(cur);
+      q += 2;
+      prefetch(cur, d);
     }
+    (void)ok;
   }
 
   tc_fence_before();
