@@ -386,7 +386,14 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
 
 // One dequant stage of the calling thread: its four rows' 16-code chunk (k-chunk t & 3 of the
 // stage's 64 k) and the scale and qbias of the group that chunk belongs to.
-constexpr int DQ_ROWS = 4;  // rows per dequant thread: 256 threads of a warp group cover 256 rows
+// Dequant warp groups taking the stages in turn.  A group's wait for B slot q % S reads the
+// barrier's phase parity, so the barrier must be at most one phase behind: the group's own
+// previous stage q - DQ_GROUPS needed stage q - DQ_GROUPS - S released, which covers q - 2S only
+// when DQ_GROUPS <= S.
+constexpr int DQ_GROUPS = 2;
+static_assert(DQ_GROUPS <= GemmCfg<true>::STAGES, "a dequant group could run a whole ring cycle ahead");
+constexpr int DQ_THREADS = 512 / DQ_GROUPS;     // threads of one group
+constexpr int DQ_ROWS = 256 / (DQ_THREADS / 4);  // B-tile rows per thread (four threads per row)
 struct DqStage {
   int4 codes[DQ_ROWS];
   float sc[DQ_ROWS], qb[DQ_ROWS];
@@ -399,7 +406,7 @@ __device__ __forceinline__ void dq_load_stage(const GemmParams& p, const uint8_t
   const int k0 = kb * 64 + kc * 16;
 #pragma unroll
   for (int i = 0; i < DQ_ROWS; ++i) {
-    const int n = (t >> 2) + 64 * i;  // row within the 256-row tile
+    const int n = (t >> 2) + (DQ_THREADS / 4) * i;  // row within the 256-row tile
     const int grow = (n < 128) ? brow0 + n : brow1 + (n - 128);
     const bool ok = grow < p.w_rows && k0 < p.K;  // K % 32 == 0: a 16-code chunk is all in or all out
     const size_t gi = static_cast<size_t>(grow) * p.groups + g;
@@ -433,15 +440,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // Dequantise one stage: the thread's codes -> bf16 [256][64] in the 128-byte swizzled K-major
-// layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).  Thread t of the 256 threads of
-// a dequant warp group handles k-chunk (t & 3) (16 codes, one group) of rows t/4 + 64 i.  Each
+// layout (row n at n*128 bytes, 16-byte chunk c at c ^ (n & 7)).  Thread t of the DQ_THREADS
+// threads of a dequant warp group handles k-chunk (t & 3) (16 codes, one group) of rows
+// t/4 + (DQ_THREADS/4) i.  Each
 // 16-byte chunk goes out as one 128-bit shared store: a quarter warp (two rows, eight chunks)
 // then covers all 32 banks once.
 __device__ __forceinline__ void dequant_stage(uint32_t sb, const DqStage& d, int t) {
   const int kc = t & 3;
 #pragma unroll
   for (int i = 0; i < DQ_ROWS; ++i) {
-    const int n = (t >> 2) + 64 * i;
+    const int n = (t >> 2) + (DQ_THREADS / 4) * i;
     const uint64_t sc2 = (static_cast<uint64_t>(__float_as_uint(d.sc[i])) << 32) | __float_as_uint(d.sc[i]);
     const uint64_t qb2 = (static_cast<uint64_t>(__float_as_uint(d.qb[i])) << 32) | __float_as_uint(d.qb[i]);
     const uint32_t cw[4] = {(uint32_t)d.codes[i].x, (uint32_t)d.codes[i].y, (uint32_t)d.codes[i].z,
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_ready + 8 * s, 8);  // the eight warps of the group that dequantises the stage
+      mbar_init(bar_ready + 8 * s, DQ_THREADS / 32);  // the warps of the group that dequantises the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
@@ -613,14 +621,14 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       }
     }
   } else if (INT8) {
-    // Two groups of eight dequant warps take the CTA's (tile, kb) stages in turn: group g
-    // dequantises stages g, g + 2, g + 4, ...  A warp loads the codes, scales and qbias of its
+    // DQ_GROUPS groups of dequant warps take the CTA's (tile, kb) stages in turn: group g
+    // dequantises stages g, g + DQ_GROUPS, g + 2 DQ_GROUPS, ...  A warp loads the codes, scales and qbias of its
     // next stage right after the proxy fence of the current one, into the registers it has just
     // consumed, and they arrive while the other group works.  So no load is in flight when a
     // warp issues its fence: the fence that hands a B tile to the tensor core waits for the
     // warp's shared stores alone.
-    const int grp = (threadIdx.x - 192) >> 8;
-    const int t = (threadIdx.x - 192) & 255;
+    const int grp = (threadIdx.x - 192) / DQ_THREADS;
+    const int t = (threadIdx.x - 192) % DQ_THREADS;
     struct Cursor {
       int tile, kb, nb;
     };
@@ -645,11 +653,8 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       int mb;
       tile_coords(cur.tile, p.m_tiles, p.n_tiles, p.group_m, mb, cur.nb);
     }
-    int q = 0;  // stage index in the CTA's sequence: ring slot q % S, phase (q / S) & 1
-    if (grp == 1) {
-      advance(cur);
-      q = 1;
-    }
+    int q = grp;  // stage index in the CTA's sequence: ring slot q % S, phase (q / S) & 1
+    for (int i = 0; i < grp; ++i) advance(cur);
     DqStage d;
     prefetch(cur, d);
     bool ok = true;
@@ -663,9 +668,8 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ready + 8 * s);
-      advance(cur);
-      advance(cur);
-      q += 2;
+      for (int i = 0; i < DQ_GROUPS; ++i) advance(cur);
+      q += DQ_GROUPS;
       prefetch(cur, d);
     }
     (void)ok;
