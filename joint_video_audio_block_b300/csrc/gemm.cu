@@ -3,7 +3,8 @@
 // y[M, n] = epilogue(x[M, K] . W[n, K]^T + b), x and W both K-major bf16 (or W as weight-only
 // INT8 group-32 codes, "mlx-h3" README, "Local model layout"), fp32 accumulation in TMEM.
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+// Design (one CTA per SM, persistent over 128 x 256 output tiles; 128 x 192 for the plain and
+// gate+residual linears when that fills the last wave of SMs better):
 //   warp 0      TMA producer: A tile 128x64 and B tile 256x64 per stage (128-byte swizzle)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer (M=128, N=256, K=16 steps)
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bias / SwiGLU / gate+residual, store
@@ -31,7 +32,6 @@ namespace h3 {
 
 constexpr int G_BM = 128, G_BN = 256, G_BK = 64;
 constexpr int G_A_BYTES = G_BM * G_BK * 2;   // 16 KB
-constexpr int G_B_BYTES = G_BN * G_BK * 2;   // 32 KB
 // Tile raster: column sweeps over groups of group_m row-blocks.  The host sizes group_m so a
 // group's A rows (group_m x 128 x K x 2 bytes) take about 24 MB of the 126 MB L2 and stay
 // resident while the sweep streams B once per group: B is read from HBM m_tiles / group_m
@@ -44,14 +44,18 @@ constexpr size_t kRasterABytes = size_t(24) << 20;
 // mainloop of the next.  INT8 weights: 256 x 256 tiles (two 128-row MMAs per k-step share each
 // dequantised B tile, halving the dequantisation per FLOP); the two accumulators fill TMEM, so
 // the epilogue does not overlap the next tile's mainloop.
-template <bool INT8>
+// bf16 weights with the plain or gate+residual epilogue may also run 128 x 192 tiles (BN = 192):
+// chosen on the host when they fill the last wave of SMs better (small row counts against the
+// 5376-wide projections), with a fifth ring stage in the shared memory the narrower B tile frees.
+template <bool INT8, int BN = G_BN>
 struct GemmCfg {
   static constexpr int BM = INT8 ? 256 : 128;
   static constexpr int MSUB = BM / 128;        // 128-row MMAs per k-step
   static constexpr int NBUF = INT8 ? 1 : 2;    // accumulator buffers
   static constexpr int A_BYTES = BM * G_BK * 2;
-  static constexpr int STAGES = INT8 ? 3 : 4;
-  static constexpr int STAGE_BYTES = A_BYTES + G_B_BYTES;
+  static constexpr int B_BYTES = BN * G_BK * 2;  // INT8: the dequantised 256-row tile
+  static constexpr int STAGES = INT8 ? 3 : (BN == G_BN ? 4 : 5);
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int THREADS = INT8 ? 192 + 32 * 16 : 192;  // INT8: 2 groups of 8 dequant warps
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 };
@@ -288,7 +292,7 @@ __device__ __forceinline__ void qkv_epilogue(const GemmParams& p, uint32_t tacc,
 // Epilogue of one tile for the calling thread's row (TMEM lane = row within the tile), CW
 // accumulator columns at a time (16 in the INT8 kernels, whose 22 warps leave 80 registers a
 // thread; 32 otherwise).
-template <int EPI, int CW>
+template <int EPI, int CW, int BN>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc, int row, int nb) {
   const bool row_ok = row < p.M;
   if (EPI == kEpiQkv) {
@@ -339,11 +343,11 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
                  static_cast<long long>(6 * t.tag[row] + p.m_gate) * p.n_y;
     }
 #pragma unroll 1
-    for (int c = 0; c < 256 / CW; ++c) {
+    for (int c = 0; c < BN / CW; ++c) {
       uint32_t r[CW];
       tmem_ld_cols<CW>(tacc + c * CW, r);
       tmem_wait_ld();
-      const int col0 = nb * 256 + c * CW;
+      const int col0 = nb * BN + c * CW;
       if (row_ok && col0 < p.n_y) {
         const int valid = min(CW, p.n_y - col0);
         float v[CW];
@@ -472,11 +476,13 @@ __device__ __forceinline__ void dequant_stage(uint32_t sb, const DqStage& d, int
   }
 }
 
-template <int EPI, bool INT8>
+template <int EPI, bool INT8, int BN = G_BN>
 __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
-  using C = GemmCfg<INT8>;
+  static_assert(BN == G_BN || (!INT8 && (EPI == kEpiBias || EPI == kEpiGateRes) && BN % 64 == 0),
+                "narrow column tiles only for bf16 weights with the plain or gate epilogue");
+  using C = GemmCfg<INT8, BN>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -536,13 +542,17 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
             break;
           }
           const uint32_t fb = bar_full + 8 * s;
-          mbar_arrive_expect_tx(fb, C::A_BYTES + (INT8 ? 0 : G_B_BYTES));
+          mbar_arrive_expect_tx(fb, C::A_BYTES + (INT8 ? 0 : C::B_BYTES));
 #pragma unroll
           for (int a = 0; a < C::MSUB; ++a)
             tma_load_2d(smem_u32(sA(s)) + a * G_A_BYTES, &tmA, fb, kb * G_BK, mb * C::BM + a * 128);
-          if (!INT8) {
+          if (!INT8 && BN == G_BN) {  // two 128-row boxes (SwiGLU: gate rows, then value rows)
             tma_load_2d(smem_u32(sB(s)), &tmB, fb, kb * G_BK, brow0);
             tma_load_2d(smem_u32(sB(s)) + 128 * 128, &tmB, fb, kb * G_BK, brow1);
+          } else if (!INT8) {  // BN / 64 boxes of 64 consecutive rows
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(smem_u32(sB(s)) + i * 64 * 128, &tmB, fb, kb * G_BK, brow0 + 64 * i);
           }
           if (++s == S) {
             s = 0;
@@ -555,7 +565,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(G_BM, G_BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(G_BM, BN);
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
@@ -565,7 +575,7 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + acc * C::MSUB * G_BN;  // accumulator a of the tile at d + a * 256
+        const uint32_t d = tmem_base + acc * C::MSUB * G_BN;  // accumulators 256 columns apart
         for (int kb = 0; kb < p.kb_count; ++kb) {
           if (!mbar_wait(bar_full + 8 * s, ph, ec, kErrGemmMma) ||
               (INT8 && !mbar_wait(bar_ready + 8 * s, ph, ec, kErrGemmMma))) {
@@ -610,7 +620,8 @@ __global__ void __launch_bounds__(GemmCfg<INT8>::THREADS, 1)
 #pragma unroll 1
       for (int a = 0; a < C::MSUB; ++a) {
         const int row = mb * C::BM + a * 128 + quad * 32 + lane;
-        gemm_epilogue<EPI, INT8 ? 16 : 32>(p, tmem_base + (acc * C::MSUB + a) * G_BN + ((quad * 32) << 16), row, nb);
+        gemm_epilogue<EPI, INT8 ? 16 : 32, BN>(p, tmem_base + (acc * C::MSUB + a) * G_BN + ((quad * 32) << 16), row,
+                                               nb);
       }
       tc_fence_before();
       __syncwarp();
@@ -720,17 +731,18 @@ int num_sms() {
   return n > 0 ? n : 148;
 }
 
-template <int EPI, bool INT8>
+template <int EPI, bool INT8, int BN = G_BN>
 static cudaError_t launch_tc(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st) {
-  using C = GemmCfg<INT8>;
+  using C = GemmCfg<INT8, BN>;
   static bool configured = false;  // per instantiation; the attribute is per function, not per device
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, INT8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<EPI, INT8, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int grid = min(p.num_tiles, num_sms());
-  gemm_tc_kernel<EPI, INT8><<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, p);
+  gemm_tc_kernel<EPI, INT8, BN><<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -742,7 +754,18 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
   p.n_y = a.n_y;
   p.m_tiles = cdiv(a.M, a.int8 ? GemmCfg<true>::BM : GemmCfg<false>::BM);
   const bool sw = a.epi == kEpiSwiglu;
-  p.b_row_step = sw ? 128 : 256;
+  // Column-tile width: 256, or 192 for the bf16 plain / gate+residual linears when that fills
+  // the SMs' last wave clearly better -- fewer column-width units per SM over the whole launch,
+  // (rounds of 148 tiles) x width, by more than 3% (the narrower tile costs some per-tile
+  // overhead).  1,829 rows x 5376 columns: 315 tiles of 256 = 3 rounds (768) against 420 of
+  // 192 = 3 rounds (576).
+  int bn = G_BN;
+  if (!a.int8 && (a.epi == kEpiBias || a.epi == kEpiGateRes)) {
+    const long long nsm = num_sms();
+    auto cost = [&](int w) { return cdiv(static_cast<long long>(p.m_tiles) * cdiv(a.n_y, w), nsm) * w; };
+    if (cost(192) * 100 < cost(G_BN) * 97) bn = 192;
+  }
+  p.b_row_step = sw ? 128 : bn;
   p.b_row1_off = sw ? a.n_y : 128;
   p.n_tiles = cdiv(a.n_y, p.b_row_step);
   p.num_tiles = p.m_tiles * p.n_tiles;
@@ -792,10 +815,12 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   } else {
-    if (!encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w, a.K, w_rows, static_cast<uint64_t>(a.K) * 2, G_BK, 128,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w, a.K, w_rows, static_cast<uint64_t>(a.K) * 2, G_BK,
+                   bn == G_BN ? 128 : 64, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  if (bn == 192) return a.epi == kEpiBias ? launch_tc<kEpiBias, false, 192>(ta, tb, p, st)
+                                          : launch_tc<kEpiGateRes, false, 192>(ta, tb, p, st);
   switch (a.epi * 2 + (a.int8 ? 1 : 0)) {
     case kEpiBias * 2: return launch_tc<kEpiBias, false>(ta, tb, p, st);
     case kEpiBias * 2 + 1: return launch_tc<kEpiBias, true>(ta, tb, p, st);
