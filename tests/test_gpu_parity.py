@@ -230,10 +230,11 @@ def _linear_case(M, K, n_out, seed=0):
 
 @pytest.mark.parametrize("flags", [0, h3.H3_F_UNFUSED])
 @pytest.mark.parametrize("M,K,n_out", [(72, 192, 768), (72, 256, 192), (1829, 5376, 21504), (300, 7168, 5376),
-                                       (1, 64, 256), (129, 96, 512), (256, 5120, 5376)])
+                                       (1, 64, 256), (129, 96, 512), (256, 5120, 5376), (300, 512, 1000)])
 def test_linear_bias(M, K, n_out, flags):
     """The bias-epilogue GEMM; (256, 5120, 5376) is the condition projection of the text rows
-    (5120-wide encoder features to the hidden width)."""
+    (5120-wide encoder features to the hidden width).  Small row counts take the 192-wide column
+    tiles; (300, 512, 1000) ends in a partial one (40 columns)."""
     if flags and M * K * n_out > 5e10:
         pytest.skip("reference kernel too slow at this size")
     x, w, b = _linear_case(M, K, n_out)
