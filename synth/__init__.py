@@ -201,6 +201,8 @@ _T77, _VIDX, _AIDX = _schedule_timesteps()
 CONFIGS = {
     "tiny": Config("tiny", TINY, Layout(16, (), 24, (2, 4, 4)), seed=0, timesteps=(0.5,)),
     "block1829": Config("block1829", H3, Layout(256, (), 37, (6, 16, 16)), seed=1),
+    # full width over a short ragged sequence: two 128-row tiles with a one-row tail
+    "block129": Config("block129", H3, Layout(64, (), 33, (1, 4, 8)), seed=8),
     "block12936": Config("block12936", H3, Layout(256, (), 200, (32, 15, 26)), seed=2),
     "block12936_int8": Config("block12936_int8", H3, Layout(256, (), 200, (32, 15, 26)), seed=3, int8=True),
     "trunk50x1829_narrow": Config(

@@ -569,6 +569,20 @@ def test_block1829_full():
     check(got, ref, emu, what="block 1829 rows")
 
 
+def test_block129_ragged_full():
+    """The full-width block over 129 rows (64 text, 33 audio, 1 x 4 x 8 video): every kernel's
+    row tiling ends in a one-row tail, and the 192-wide column tiles serve O and fc2."""
+    c = Case("block129")
+    assert c.n == 129
+    wt = R.upload_block(c.w_bits[0])
+    out = torch.empty_like(c.x)
+    _run_block(c, wt, c.x, out)
+    ref = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d)
+    got = R.f32_from_bf16(out)
+    emu = O.block_forward(c.x_bits, c.w_bits[0], c.table_b(0), c.tag, c.tidx, c.pos, c.d, emulate_bf16=True)
+    check(got, ref, emu, what="block 129 rows")
+
+
 @pytest.mark.parametrize("name", ["block12936", "block12936_int8"])
 def test_block12936_sampled(name):
     c = Case(name)
