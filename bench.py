@@ -283,6 +283,59 @@ def time_single_blocks(dev, sp, reps=20, warmup=5):
     return out
 
 
+# The pages' own figure for the 37,966-row request: 8.8 min per 50-block denoising step on an M3
+# Ultra (MLX, bf16, one block timed and multiplied by 50; "minimax-h3-mlx" README, "Performance").
+# Another machine's number: context for the page-faithful canvas, not a target.
+PAGES_M3_ULTRA_STEP_S = 8.8 * 60
+
+
+def time_page_canvas(dev, sp, dims, bws, B, table, T, steps=2, warmup=1):
+    """The same 50-block trunk (the resident weights and modulation table of the main workload)
+    over the pages' 5 s, 1344x768 request: 37,966 packed rows, tokens/s per denoiser step, next
+    to the pages' M3 Ultra figure for that request."""
+    import torch
+
+    from joint_video_audio_block_b300 import h3
+    from joint_video_audio_block_b300 import runtime as R
+
+    cfg = synth.CONFIGS["trunk37966"]
+    d = cfg.dims
+    N = cfg.layout.n_rows
+    tag, tidx, pos = (torch.from_numpy(a).to(dev) for a in synth.packed_rows(cfg, step=10))
+    x0 = synth.device_normal_bf16(cfg.seed, 0xFFFF03, (N, d.hidden))
+    x = torch.empty_like(x0)
+    ws = R.workspace(dims, N)
+
+    def step():
+        x.copy_(x0)
+        h3.h3_trunk_forward(dims, bws, B, table.data_ptr(), T, x.data_ptr(), N, tag.data_ptr(), tidx.data_ptr(),
+                            pos.data_ptr(), ws.data_ptr(), ws.numel(), 0, sp)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    st, site = h3.h3_last_device_error(sp)
+    if st != h3.H3_OK:
+        raise RuntimeError(f"device error timing the page canvas: site {site:#x}")
+    s_per_step = e0.elapsed_time(e1) / 1e3 / steps
+    lay = cfg.layout
+    out = {"workload": cfg.name, "rows": N,
+           "layout": f"text {lay.text} | audio {lay.audio} | video {'x'.join(map(str, lay.video))} "
+                     "(a reading: the pages give only the total)",
+           "blocks": B, "steps": steps, "ms_per_step": s_per_step * 1e3, "tokens_per_s": N / s_per_step,
+           "pages_figure": {"s_per_step": PAGES_M3_ULTRA_STEP_S, "tokens_per_s": N / PAGES_M3_ULTRA_STEP_S,
+                            "hardware": "M3 Ultra, MLX, bf16", "use": "context, another machine"}}
+    del x0, x, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, cfg, rank, world, local_rank):
     import torch
 
@@ -433,6 +486,9 @@ def run_ours(args, cfg, rank, world, local_rank):
     mma_tflops = B * (lin_f + att_f) / (ms_per_step / 1e3) / 1e12  # per GPU (each replica)
     traffic = _attention_traffic(N)
 
+    canvas = None
+    if not args.no_page_canvas and cfg.name == "trunk33720" and B == cfg.n_blocks:
+        canvas = time_page_canvas(dev, sp, dims, bws, B, table, T)
     blocks_timed = None if args.no_block_workloads else time_single_blocks(dev, sp)
 
     cpu = None
@@ -462,6 +518,7 @@ def run_ours(args, cfg, rank, world, local_rank):
             "sampler_transition": {"ms": transition_ms, "tokens_per_s": N / (transition_ms / 1e3),
                                    "what": "entry projections + trunk + output heads + Euler (h3_denoise_step)"},
             "single_block_workloads": blocks_timed,
+            "page_canvas": canvas,
             "gpu_launches": args.steps * (1 + 7 * B),  # rope table + 7 kernels per block
             "clocks": clk,
             "cpu_baseline": cpu,
@@ -482,6 +539,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-block-workloads", action="store_true",
                     help="skip the per-block timings of the 1,829- and 12,936-row configurations")
+    ap.add_argument("--no-page-canvas", action="store_true",
+                    help="skip the pages' 37,966-row request (timed after the main workload)")
     ap.add_argument("--clocks-csv", default=None, help="where to keep the raw clock samples ({rank} is replaced)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))

@@ -215,6 +215,13 @@ CONFIGS = {
         "trunk50x1829", H3, Layout(256, (), 37, (6, 16, 16)), seed=6, n_blocks=50, n_timesteps=77,
         timesteps=_T77,
     ),
+    # the pages' 5 s, 1344x768 request ("minimax-h3-mlx" README, "Performance": 37,966 packed
+    # rows, the workload of the M3 Ultra per-block and per-step figures).  The pages give only
+    # the total; the split is a reading: 37 latent frames of 24 x 42, 200 audio rows, 470 text rows.
+    "trunk37966": Config(
+        "trunk37966", H3, Layout(470, (), 200, (37, 24, 42)), seed=9, n_blocks=50, n_timesteps=77,
+        timesteps=_T77,
+    ),
     "trunk33720": Config(
         "trunk33720", H3, Layout(256, (24, 42), 200, (32, 24, 42)), seed=4, n_blocks=50, n_timesteps=77,
         timesteps=_T77,
