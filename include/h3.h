@@ -10,7 +10,9 @@
  * IEEE bfloat16 bit patterns (2 bytes), "f32" float32.
  *
  * Errors: every call returns an h3_status.  Shape, alignment and null-pointer violations are
- * detected on the host and return H3_EINVAL before anything is launched; a CUDA launch error
+ * detected on the host and return H3_EINVAL before anything is launched (bf16 tensors the
+ * kernels move in 16-byte vectors must be 16-byte aligned where an entry point says so; every
+ * f32 and i32 array must be 4-byte aligned); a CUDA launch error
  * returns H3_ECUDA.  Kernels never trap: a pipeline wait that exceeds its time limit records a
  * site code in the library's device error word and ends the launch; h3_last_device_error()
  * reports it.  Nothing aborts the process.

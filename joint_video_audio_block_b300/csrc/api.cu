@@ -47,6 +47,8 @@ unsigned* error_word() {
 
 static size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+// int32 / float32 arrays the kernels read element-wise (tidx, pos, latents): 4-byte aligned
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 static int ld_vt_for(int n_rows) { return (n_rows + 63) / 64 * 64; }
 
 struct Workspace {
@@ -299,7 +301,7 @@ h3_status h3_adaln_modulate(const h3_dims* dims, const void* x, void* xn, int n_
                             void* stream) {
   if (!dims_ok(dims) || n_rows < 0 || !x || !xn || x == xn || !table_b || !tag || !tidx) return H3_EINVAL;
   if (m_shift < 0 || m_shift > 5 || m_scale < 0 || m_scale > 5 || !aligned16(x) || !aligned16(xn) ||
-      !aligned16(table_b) || t_stride % 8)
+      !aligned16(table_b) || t_stride % 8 || !aligned4(tidx))
     return H3_EINVAL;
   TableRef tr{static_cast<const bf16*>(table_b), t_stride, tag, tidx};
   return cuda_status(launch_adaln_modulate(static_cast<const bf16*>(x), static_cast<bf16*>(xn), n_rows,
@@ -319,7 +321,7 @@ h3_status h3_linear_forward(const h3_linear* lin, int epilogue, const void* x, i
   LinearArgs a = make_linear(*lin, epilogue, static_cast<const bf16*>(x), lda, static_cast<bf16*>(y), ldy, n_rows);
   if (epilogue == H3_EPI_GATE_RES) {
     if (!res || !table_b || !tag || !tidx || m_gate < 0 || m_gate > 5 || !aligned16(res) || !aligned16(table_b) ||
-        t_stride % 8)
+        t_stride % 8 || !aligned4(tidx))
       return H3_EINVAL;
     a.res = static_cast<const bf16*>(res);
     a.gate = TableRef{static_cast<const bf16*>(table_b), t_stride, tag, tidx};
@@ -409,7 +411,7 @@ h3_status h3_block_forward(const h3_dims* dims, const h3_block_w* w, const void*
   if (!dims_ok(dims) || !block_w_ok(*dims, w) || !table_b || T <= 0 || t_stride % 8 || !x_in || !x_out ||
       n_rows < 0 || !tag || !tidx || !pos || !workspace)
     return H3_EINVAL;
-  if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(table_b) ||
+  if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(table_b) || !aligned4(tidx) || !aligned4(pos) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255))
     return H3_EINVAL;
   if (x_in != x_out) {
@@ -434,7 +436,9 @@ h3_status h3_trunk_forward(const h3_dims* dims, const h3_block_w* blocks, int n_
   if (!dims_ok(dims) || !blocks || n_blocks <= 0 || !table || T <= 0 || !x || n_rows < 0 || !tag || !tidx || !pos ||
       !workspace)
     return H3_EINVAL;
-  if (!aligned16(x) || !aligned16(table) || (reinterpret_cast<uintptr_t>(workspace) & 255)) return H3_EINVAL;
+  if (!aligned16(x) || !aligned16(table) || !aligned4(tidx) || !aligned4(pos) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return H3_EINVAL;
   for (int b = 0; b < n_blocks; ++b)
     if (!block_w_ok(*dims, &blocks[b])) return H3_EINVAL;
   const Workspace ws = plan(*dims, n_rows, workspace);
@@ -470,6 +474,14 @@ h3_status denoise_entry_trunk(const h3_dims* dims, const h3_block_w* blocks, int
   const int L = io->text_rows, C = io->cond_rows, A = io->audio_rows, V = io->video_rows;
   if (L < 0 || C < 0 || A < 0 || V < 0 || (L && !text_x) || (C && !z_cond) || (A && !z_audio) || (V && !z_video))
     return H3_EINVAL;
+  // everything the entry projections and heads read, checked before the first launch
+  const void* f32s[] = {z_cond, z_video, z_audio, io->patch_v, io->patch_v_b, io->patch_a, io->patch_a_b,
+                        io->head_v, io->head_v_b, io->head_a, io->head_a_b};
+  for (const void* f : f32s)
+    if (!aligned4(f)) return H3_EINVAL;
+  if (((C || V) && (!io->patch_v || !io->head_v)) || (A && (!io->patch_a || !io->head_a))) return H3_EINVAL;
+  if (io->k_video <= 0 || io->k_video > 128 || io->k_audio <= 0 || io->k_audio > 128) return H3_EINVAL;
+  if (!aligned16(table_f) || (L && !aligned16(text_x))) return H3_EINVAL;
   const int n = L + C + A + V;
   const size_t row_bytes = static_cast<size_t>(H) * 2;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -521,6 +533,8 @@ h3_status h3_denoise_step_ms(const h3_dims* dims, const h3_block_w* blocks, int 
                              const h3_ms_step* step_audio, void* workspace, size_t ws_bytes, unsigned flags,
                              void* stream) {
   if (!io || !step_video || !step_audio || (io->audio_rows && !d_prev_audio) || (io->video_rows && !d_prev_video))
+    return H3_EINVAL;
+  if (!aligned4(d_prev_video) || !aligned4(d_prev_audio) || !(step_video->sigma > 0.f) || !(step_audio->sigma > 0.f))
     return H3_EINVAL;
   h3_status s = denoise_entry_trunk(dims, blocks, n_blocks, table, table_f, T, io, text_x, z_cond, z_video, z_audio,
                                     x, tag, tidx, pos, workspace, ws_bytes, flags, stream);

@@ -231,13 +231,14 @@ using namespace h3;
 
 namespace {
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool a4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }  // float32 / int32 arrays
 }  // namespace
 
 extern "C" h3_status h3_embed_rows(const h3_dims* dims, const float* z, int K, const float* w, const float* b,
                                    int n_rows, void* x_rows, void* stream) {
   if (!dims || !z || !w || !x_rows || K <= 0 || K > 4096 || n_rows < 0) return H3_EINVAL;
   const int H = dims->hidden;
-  if (H <= 0 || H % 64 || !a16(x_rows)) return H3_EINVAL;
+  if (H <= 0 || H % 64 || !a16(x_rows) || !a4(z) || !a4(w) || !a4(b)) return H3_EINVAL;
   if (n_rows == 0) return H3_OK;
   dim3 grid(cdiv(H, EM_COLS), cdiv(n_rows, EM_ROWS));
   embed_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(z, K, w, b, n_rows, H, static_cast<bf16*>(x_rows));
@@ -253,6 +254,9 @@ h3_status launch_head(const h3_dims* dims, const void* x_rows, int n_rows, const
   if (!v_out && !z_inout) return H3_EINVAL;
   const int H = dims->hidden;
   if (H <= 0 || H % 64 || !a16(x_rows) || t_stride < 6LL * H) return H3_EINVAL;
+  if (!a4(tidx) || !a4(w) || !a4(b) || !a4(v_out) || !a4(z_inout) || !a4(d_prev) ||
+      (reinterpret_cast<uintptr_t>(table_f) & 1))
+    return H3_EINVAL;
   if (ms && (!z_inout || !d_prev || !(ms->sigma > 0.f))) return H3_EINVAL;
   if (n_rows == 0) return H3_OK;
   HeadArgs a{static_cast<const bf16*>(x_rows), n_rows, H, tag, tidx, static_cast<const bf16*>(table_f), t_stride,

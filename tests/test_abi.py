@@ -22,6 +22,21 @@ def h3mod():
     return h3
 
 
+def _no_gpu() -> bool:
+    try:
+        import torch
+
+        return not torch.cuda.is_available()
+    except ImportError:  # pragma: no cover
+        return True
+
+
+# Tests that hand the library fake device addresses rely on the host checks refusing the call
+# before any launch; they run only where no GPU exists, so a regressed check can never turn
+# into a launch on those addresses.
+fake_addresses = pytest.mark.skipif(not _no_gpu(), reason="fake device addresses: host-only test")
+
+
 def _declared():
     text = open(HEADER).read()
     return sorted(set(re.findall(r"^\s*(?:h3_status|size_t|const char\s*\*)\s+(h3_\w+)\s*\(", text, re.M)))
@@ -75,6 +90,7 @@ def test_workspace_plan(h3mod):
     assert h3mod.h3_workspace_size(bad, 72) == 0
 
 
+@fake_addresses
 def test_invalid_arguments_rejected_before_launch(h3mod):
     """Null pointers and inconsistent shapes return H3_EINVAL on the host: no CUDA call runs."""
     L = h3mod.lib()
@@ -106,6 +122,7 @@ def test_sigma_schedule_is_the_oracle_grid(h3mod):
         np.testing.assert_array_equal(got, O.shifted_sigmas(steps, shift))
 
 
+@fake_addresses
 def test_more_invalid_arguments_rejected_before_launch(h3mod):
     """Misalignment and range errors of the newer entry points are refused on the host."""
     L = h3mod.lib()
@@ -140,6 +157,7 @@ def test_more_invalid_arguments_rejected_before_launch(h3mod):
     assert L.h3_kernel_timer_start(-1) == h3mod.H3_EINVAL
 
 
+@fake_addresses
 def test_qknorm_rope_entry_points_refuse_misaligned_pointers(h3mod):
     """Both QK-norm + RoPE entry points refuse, on the host, any pointer the kernel would access
     with a vector width it is not aligned to (qkv, q_out, k_out, vt_out: 16 bytes; pos: 4), and
@@ -178,6 +196,7 @@ def test_qknorm_rope_entry_points_refuse_misaligned_pointers(h3mod):
             h3mod.H3_EINVAL
 
 
+@fake_addresses
 def test_modcache_build_refuses_misaligned_inputs(h3mod):
     """The table build reads the embedding by TMA (16-byte aligned rows) and the weights by TMA
     (16-byte aligned base): a misaligned embedding, weight or bias pointer, or an embedding
@@ -221,6 +240,7 @@ def test_res_multistep_weights_are_the_oracle_s_rounded_to_float(h3mod):
                 assert got.c_prev == 0.0
 
 
+@fake_addresses
 def test_res_multistep_arguments_refused(h3mod):
     L = h3mod.lib()
     out = h3mod.h3_ms_step()
@@ -238,4 +258,67 @@ def test_res_multistep_arguments_refused(h3mod):
     assert L.h3_head_forward_ms(ctypes.byref(d), al, 8, al, al, al, 6 * 192, al, None, 96, ctypes.byref(step), al,
                                 None, al, None) == h3mod.H3_EINVAL
     assert L.h3_head_forward_ms(ctypes.byref(d), al, 8, al, al, al, 6 * 192, al, None, 96, None, None, al, al,
+                                None) == h3mod.H3_EINVAL
+
+
+@fake_addresses
+def test_misaligned_int32_and_float32_arrays_refused(h3mod):
+    """Every f32 / i32 array a kernel reads element by element must be 4-byte aligned; an array
+    that is not returns H3_EINVAL on the host (the fake addresses below are never touched: each
+    call must refuse first).  Covers tidx and pos of the block and trunk, the gate's tidx, the
+    AdaLN tidx, the entry projection and head arrays, and both sampler transitions."""
+    L = h3mod.lib()
+    d = _tiny_dims(h3mod)
+    al, odd = 0x40000, 0x40002  # 16-byte aligned; 2 bytes off
+    H, I, F = 192, 256, 512
+
+    def lin(n_out, k):
+        x = h3mod.h3_linear()
+        x.fmt, x.w, x.n_out, x.k = 0, al, n_out, k
+        return x
+
+    bw = h3mod.h3_block_w()
+    bw.qkv, bw.o, bw.fc1, bw.fc2 = lin(3 * I, H), lin(H, I), lin(2 * F, H), lin(H, F)
+    ws = 0x100000
+    big = 1 << 30
+    for tidx, pos in ((odd, al), (al, odd)):
+        assert L.h3_block_forward(ctypes.byref(d), ctypes.byref(bw), al, 18 * H, 1, al, al, 72, al, tidx, pos, ws, big,
+                                  0, None) == h3mod.H3_EINVAL
+        assert L.h3_trunk_forward(ctypes.byref(d), ctypes.byref(bw), 1, al, 1, al, 72, al, tidx, pos, ws, big, 0,
+                                  None) == h3mod.H3_EINVAL
+    assert L.h3_adaln_modulate(ctypes.byref(d), al, al + 0x10000, 72, al, 18 * H, 0, 1, al, odd, None) == h3mod.H3_EINVAL
+    lo = lin(H, I)
+    assert L.h3_linear_forward(ctypes.byref(lo), h3mod.H3_EPI_GATE_RES, al, I, al, H, 72, al, al, 18 * H, 2, al, odd, 0,
+                               None) == h3mod.H3_EINVAL
+    f = ctypes.c_float
+    # entry projection: latents, weights, bias
+    for z, w, b in ((odd, al, al), (al, odd, al), (al, al, odd)):
+        assert L.h3_embed_rows(ctypes.byref(d), z, 96, w, b, 8, al, None) == h3mod.H3_EINVAL
+    # head: tidx, weights, bias, v, z (Euler); and the previous prediction (res_multistep)
+    for tidx, w, b, v, z in ((odd, al, al, al, al), (al, odd, al, al, al), (al, al, odd, al, al),
+                             (al, al, al, odd, al), (al, al, al, al, odd)):
+        assert L.h3_head_forward(ctypes.byref(d), al, 8, al, tidx, al, 6 * H, w, b, 96, v, z, f(-0.1),
+                                 None) == h3mod.H3_EINVAL
+    step = h3mod.h3_res_multistep_step(None, 0.5, 0.25)
+    assert L.h3_head_forward_ms(ctypes.byref(d), al, 8, al, al, al, 6 * H, al, al, 96, ctypes.byref(step), None, al,
+                                odd, None) == h3mod.H3_EINVAL
+    # sampler transitions: a misaligned latent array or weight is refused before the entry
+    # projections or the trunk launch
+    io = h3mod.h3_io_w()
+    io.text_rows, io.cond_rows, io.audio_rows, io.video_rows, io.k_video, io.k_audio = 8, 0, 8, 8, 96, 32
+    for fld in ("patch_v", "patch_v_b", "patch_a", "patch_a_b", "head_v", "head_v_b", "head_a", "head_a_b"):
+        setattr(io, fld, al)
+    arr = (h3mod.h3_block_w * 1)(bw)
+    for zv, za in ((odd, al), (al, odd)):
+        assert L.h3_denoise_step(ctypes.byref(d), arr, 1, al, al, 1, ctypes.byref(io), al, None, zv, za, al, al, al,
+                                 al, f(-0.1), f(-0.1), ws, big, 0, None) == h3mod.H3_EINVAL
+        assert L.h3_denoise_step_ms(ctypes.byref(d), arr, 1, al, al, 1, ctypes.byref(io), al, None, zv, za, al, al,
+                                    al, al, al, al, ctypes.byref(step), ctypes.byref(step), ws, big, 0,
+                                    None) == h3mod.H3_EINVAL
+    io.head_a = odd
+    assert L.h3_denoise_step(ctypes.byref(d), arr, 1, al, al, 1, ctypes.byref(io), al, None, al, al, al, al, al, al,
+                             f(-0.1), f(-0.1), ws, big, 0, None) == h3mod.H3_EINVAL
+    io.head_a = al
+    assert L.h3_denoise_step_ms(ctypes.byref(d), arr, 1, al, al, 1, ctypes.byref(io), al, None, al, al, odd, al, al,
+                                al, al, al, ctypes.byref(step), ctypes.byref(step), ws, big, 0,
                                 None) == h3mod.H3_EINVAL
