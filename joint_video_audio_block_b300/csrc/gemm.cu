@@ -388,8 +388,6 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& p, uint32_t tacc
   }
 }
 
-// One dequant stage of the calling thread: its four rows' 16-code chunk (k-chunk t & 3 of the
-// stage's 64 k) and the scale and qbias of the group that chunk belongs to.
 // Dequant warp groups taking the stages in turn.  A group's wait for B slot q % S reads the
 // barrier's phase parity, so the barrier must be at most one phase behind: the group's own
 // previous stage q - DQ_GROUPS needed stage q - DQ_GROUPS - S released, which covers q - 2S only
@@ -398,6 +396,9 @@ constexpr int DQ_GROUPS = 2;
 static_assert(DQ_GROUPS <= GemmCfg<true>::STAGES, "a dequant group could run a whole ring cycle ahead");
 constexpr int DQ_THREADS = 512 / DQ_GROUPS;     // threads of one group
 constexpr int DQ_ROWS = 256 / (DQ_THREADS / 4);  // B-tile rows per thread (four threads per row)
+
+// One dequant stage of the calling thread: its rows' 16-code chunk (k-chunk t & 3 of the
+// stage's 64 k) and the scale and qbias of the group that chunk belongs to.
 struct DqStage {
   int4 codes[DQ_ROWS];
   float sc[DQ_ROWS], qb[DQ_ROWS];
