@@ -98,6 +98,35 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// The 128-byte-swizzled K-major shared-memory descriptor split in two 32-bit words: the low
+// word carries the start address (16-byte units) and the unused leading offset, the high word
+// the 1024-byte stride, the descriptor version and the swizzle mode, and is the same for every
+// operand here.  The issuer keeps only low words and steps them by the k slice's offset.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+constexpr uint32_t AT_SDESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+__device__ __forceinline__ void umma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %5};\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AT_SDESC_HI)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AT_SDESC_HI)
+      : "memory");
+}
+
 // SPARSE: block-sparse attention over 128 x 128 (query tile, key tile) blocks.  mask[h][qi][kj]
 // != 0 keeps key tile kj for query tile qi of head h; every other score is -inf.  The CTA
 // loads the key tiles either of its two query tiles keeps, and each query tile multiplies and
@@ -213,21 +242,24 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD);
       // it = position of the key tile in the CTA's visiting order (selects ring stage and phase)
+      // Descriptors are built once per operand tile and stepped by the (compile-time) byte
+      // offset of each 16-wide k slice: the start-address field holds the shared address in
+      // 16-byte units, and no tile crosses 256 KB, so the step is a plain add.
       auto issue_s = [&](int x, int it) {  // S_x = Q_x K^T for visited tile it
-        const uint32_t kb = sK + (it % ST) * C::QK_TILE, qb = sQ + x * C::QK_TILE;
+        const uint32_t dq = sdesc_lo(sQ + x * C::QK_TILE), dk = sdesc_lo(sK + (it % ST) * C::QK_TILE);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * AT_ATOM + (kk & 3) * 32;
-          umma_bf16_ss(tmem + x * 128, sdesc_k_sw128(qb + off), sdesc_k_sw128(kb + off), idesc_s, kk != 0);
+          const uint32_t off = ((kk >> 2) * AT_ATOM + (kk & 3) * 32) >> 4;
+          umma_ss_lo(tmem + x * 128, dq + off, dk + off, idesc_s, kk != 0);
         }
         umma_commit(b_sfull + 8 * x);
       };
       auto issue_pv = [&](int x, int it, int first) {  // O_x (+)= P_x V for visited tile it
-        const uint32_t vb = sV + (it % ST) * C::V_TILE;
+        const uint32_t dv = sdesc_lo(sV + (it % ST) * C::V_TILE);
 #pragma unroll
         for (int kk = 0; kk < AT_BN / 16; ++kk)
-          umma_bf16_ts(tmem + 256 + x * HD, tmem + x * 128 + kk * 8,
-                       sdesc_k_sw128(vb + (kk >> 2) * C::V_ATOM + (kk & 3) * 32), idesc_o, !(first && kk == 0));
+          umma_ts_lo(tmem + 256 + x * HD, tmem + x * 128 + kk * 8,
+                     dv + (((kk >> 2) * C::V_ATOM + (kk & 3) * 32) >> 4), idesc_o, !(first && kk == 0));
       };
       // Each query tile runs its own sequence over the key tiles it keeps (all of them when
       // dense); cnt[x] counts tile x's S / P phases.  S_x of the next kept tile is issued right
