@@ -127,6 +127,71 @@ __device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// A run of MMAs over consecutive 16-wide k slices of one tile pair, in one asm block: one
+// predicate for the first MMA (accumulate or overwrite), the rest accumulate; slice i steps the
+// descriptors' low words by O_i (16-byte units, compile-time).  SS: A and B in shared memory,
+// with the same offsets (Q and K tiles share their layout).  TS: A (P) in TMEM, 8 columns per
+// slice, B (V^T) in shared memory.
+#define AT_SS_STEP(o)                                                                      \
+  "add.u32 ra, %1, " #o ";\n\tadd.u32 rb, %2, " #o ";\n\t"                               \
+  "mov.b64 da, {ra, %5};\n\tmov.b64 db, {rb, %5};\n\t"                                  \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, pt;\n\t"
+#define AT_TS_STEP(ta, o)                                                                  \
+  "add.u32 ra, %1, " #ta ";\n\tadd.u32 rb, %2, " #o ";\n\t"                              \
+  "mov.b64 db, {rb, %5};\n\t"                                                            \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], db, %3, pt;\n\t"
+#define AT_RUN_HEAD                                                                        \
+  "{\n\t.reg .pred p, pt;\n\t.reg .b32 ra, rb;\n\t.reg .b64 da, db;\n\t"                 \
+  "setp.ne.u32 p, %4, 0;\n\tsetp.eq.u32 pt, %4, %4;\n\t"
+
+// S = Q K^T over head_dim 128 (8 slices; the second four in the next 64-column swizzle atom)
+__device__ __forceinline__ void umma_ss_run8(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(AT_RUN_HEAD
+               "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t"
+               AT_SS_STEP(2) AT_SS_STEP(4) AT_SS_STEP(6) AT_SS_STEP(1024) AT_SS_STEP(1026) AT_SS_STEP(1028)
+               AT_SS_STEP(1030) "}"
+               ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AT_SDESC_HI)
+               : "memory");
+}
+// S = Q K^T over head_dim 64 (4 slices)
+__device__ __forceinline__ void umma_ss_run4(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(AT_RUN_HEAD
+               "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t"
+               AT_SS_STEP(2) AT_SS_STEP(4) AT_SS_STEP(6) "}"
+               ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AT_SDESC_HI)
+               : "memory");
+}
+// O += P V over 128 keys (8 slices); the V^T tile's second 64-key atom starts VA units on
+template <int VA>
+__device__ __forceinline__ void umma_ts_run8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate);
+template <>
+__device__ __forceinline__ void umma_ts_run8<1024>(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(AT_RUN_HEAD
+               "mov.b64 db, {%2, %5};\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t"
+               AT_TS_STEP(8, 2) AT_TS_STEP(16, 4) AT_TS_STEP(24, 6) AT_TS_STEP(32, 1024) AT_TS_STEP(40, 1026)
+               AT_TS_STEP(48, 1028) AT_TS_STEP(56, 1030) "}"
+               ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AT_SDESC_HI)
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void umma_ts_run8<512>(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(AT_RUN_HEAD
+               "mov.b64 db, {%2, %5};\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t"
+               AT_TS_STEP(8, 2) AT_TS_STEP(16, 4) AT_TS_STEP(24, 6) AT_TS_STEP(32, 512) AT_TS_STEP(40, 514)
+               AT_TS_STEP(48, 516) AT_TS_STEP(56, 518) "}"
+               ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AT_SDESC_HI)
+               : "memory");
+}
+
 // SPARSE: block-sparse attention over 128 x 128 (query tile, key tile) blocks.  mask[h][qi][kj]
 // != 0 keeps key tile kj for query tile qi of head h; every other score is -inf.  The CTA
 // loads the key tiles either of its two query tiles keeps, and each query tile multiplies and
@@ -245,21 +310,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // Descriptors are built once per operand tile and stepped by the (compile-time) byte
       // offset of each 16-wide k slice: the start-address field holds the shared address in
       // 16-byte units, and no tile crosses 256 KB, so the step is a plain add.
+      static_assert(AT_ATOM >> 4 == 1024 && (HD == 128 || HD == 64), "offsets in the MMA runs");
       auto issue_s = [&](int x, int it) {  // S_x = Q_x K^T for visited tile it
         const uint32_t dq = sdesc_lo(sQ + x * C::QK_TILE), dk = sdesc_lo(sK + (it % ST) * C::QK_TILE);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * AT_ATOM + (kk & 3) * 32) >> 4;
-          umma_ss_lo(tmem + x * 128, dq + off, dk + off, idesc_s, kk != 0);
-        }
+        if constexpr (HD == 128) umma_ss_run8(tmem + x * 128, dq, dk, idesc_s, 0);
+        else umma_ss_run4(tmem + x * 128, dq, dk, idesc_s, 0);
         umma_commit(b_sfull + 8 * x);
       };
       auto issue_pv = [&](int x, int it, int first) {  // O_x (+)= P_x V for visited tile it
         const uint32_t dv = sdesc_lo(sV + (it % ST) * C::V_TILE);
-#pragma unroll
-        for (int kk = 0; kk < AT_BN / 16; ++kk)
-          umma_ts_lo(tmem + 256 + x * HD, tmem + x * 128 + kk * 8,
-                     dv + (((kk >> 2) * C::V_ATOM + (kk & 3) * 32) >> 4), idesc_o, !(first && kk == 0));
+        umma_ts_run8<(C::V_ATOM >> 4)>(tmem + 256 + x * HD, tmem + x * 128, dv, idesc_o, !first);
       };
       // Each query tile runs its own sequence over the key tiles it keeps (all of them when
       // dense); cnt[x] counts tile x's S / P phases.  S_x of the next kept tile is issued right
