@@ -87,45 +87,12 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread (A: 128 lanes x K/2 columns of bf16 pairs)
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // The 128-byte-swizzled K-major shared-memory descriptor split in two 32-bit words: the low
 // word carries the start address (16-byte units) and the unused leading offset, the high word
 // the 1024-byte stride, the descriptor version and the swizzle mode, and is the same for every
-// operand here.  The issuer keeps only low words and steps them by the k slice's offset.
+// operand here.  The issuer keeps only low words and steps them by each k slice's offset.
 __device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
 constexpr uint32_t AT_SDESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
-
-__device__ __forceinline__ void umma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
-      "mov.b64 da, {%1, %5};\n\t"
-      "mov.b64 db, {%2, %5};\n\t"
-      "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AT_SDESC_HI)
-      : "memory");
-}
-__device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
-      "mov.b64 db, {%2, %5};\n\t"
-      "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(AT_SDESC_HI)
-      : "memory");
-}
 
 // A run of MMAs over consecutive 16-wide k slices of one tile pair, in one asm block: one
 // predicate for the first MMA (accumulate or overwrite), the rest accumulate; slice i steps the
