@@ -757,9 +757,9 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t st) {
   const bool sw = a.epi == kEpiSwiglu;
   // Column-tile width: 256, or 192 for the bf16 plain / gate+residual linears when that fills
   // the SMs' last wave clearly better -- fewer column-width units per SM over the whole launch,
-  // (rounds of 148 tiles) x width, by more than 3% (the narrower tile costs some per-tile
-  // overhead).  1,829 rows x 5376 columns: 315 tiles of 256 = 3 rounds (768) against 420 of
-  // 192 = 3 rounds (576).
+  // (whole waves of 148 tiles) x width, by more than 3% (the narrower tile costs some per-tile
+  // overhead).  1,829 rows x 5376 columns: 315 tiles of 256 = 3 waves (768) against 420 of
+  // 192 = 3 waves (576).
   int bn = G_BN;
   if (!a.int8 && (a.epi == kEpiBias || a.epi == kEpiGateRes)) {
     const long long nsm = num_sms();
