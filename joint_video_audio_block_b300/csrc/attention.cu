@@ -10,6 +10,9 @@
 //   warp 1       TMEM allocator + single-thread MMA issuer, per key tile j:
 //                  O_A += P_A(j) V_j   (A operand P from TMEM)      S_A(j+1) = Q_A K_{j+1}^T
 //                  O_B += P_B(j) V_j                                S_B(j+1) = Q_B K_{j+1}^T
+//                each a run of 8 MMAs issued as one asm block; the issuer shares its
+//                sub-partition with two softmax warps, so its own instruction count shows in
+//                the kernel's time
 //   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B: one thread per query row
 //                (its TMEM lane); the row of S is read with tcgen05.ld, the online max / sum
 //                kept in fp32, and P rounded to bf16 written back over the front half of the
@@ -273,10 +276,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD);
-      // it = position of the key tile in the CTA's visiting order (selects ring stage and phase)
-      // Descriptors are built once per operand tile and stepped by the (compile-time) byte
-      // offset of each 16-wide k slice: the start-address field holds the shared address in
-      // 16-byte units, and no tile crosses 256 KB, so the step is a plain add.
+      // Descriptors are built once per operand tile (their low words) and stepped inside the MMA
+      // runs by the compile-time offset of each 16-wide k slice: the start-address field holds
+      // the shared address in 16-byte units, and no tile crosses 256 KB, so the step is a plain
+      // add.  it = position of the key tile in the CTA's visiting order (ring stage and phase).
       static_assert(AT_ATOM >> 4 == 1024 && (HD == 128 || HD == 64), "offsets in the MMA runs");
       auto issue_s = [&](int x, int it) {  // S_x = Q_x K^T for visited tile it
         const uint32_t dq = sdesc_lo(sQ + x * C::QK_TILE), dk = sdesc_lo(sK + (it % ST) * C::QK_TILE);
