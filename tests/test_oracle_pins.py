@@ -681,6 +681,17 @@ def test_res_multistep_hand_worked_weights(sig, want):
     assert abs(sum(got) - 1.0) < 1e-14
 
 
+def test_data_prediction_recovers_the_clean_latent():
+    """Rectified flow: z = (1 - sigma) x0 + sigma eps moves with velocity v = eps - x0, so the
+    prediction z - sigma v is x0 itself, at every sigma (and a wrong sign or a (1 - sigma)
+    factor would miss it)."""
+    rng = np.random.default_rng(34)
+    x0, eps = rng.standard_normal((5, 7)), rng.standard_normal((5, 7))
+    for sigma in (1.0, 0.73, 0.2, 1e-3):
+        z = (1.0 - sigma) * x0 + sigma * eps
+        np.testing.assert_allclose(O.data_prediction(z, eps - x0, sigma), x0, rtol=0, atol=1e-14)
+
+
 def test_res_multistep_first_step_is_euler_and_last_step_is_the_prediction():
     rng = np.random.default_rng(31)
     z, v = rng.standard_normal((7, 5)), rng.standard_normal((7, 5))
