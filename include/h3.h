@@ -190,6 +190,15 @@ h3_status h3_head_forward_ms(const h3_dims* dims, const void* x_rows, int n_rows
  * sigma_out: host f32 [steps + 1]. */
 h3_status h3_sigma_schedule(int steps, float shift, float* sigma_out);
 
+/* HOST: the plan of a run with video and audio on their own grids (h3_sigma_schedule with
+ * shift_video, shift_audio): the distinct timesteps 1000 sigma (float32) that its `steps`
+ * transitions evaluate, in descending order -- the rows of the modulation tables -- and, per
+ * transition i, the row of the video (vidx[i]) and audio (aidx[i]) timestep.  Values are
+ * distinct by exact float32 equality.  timesteps: host f32 with room for 2*steps values;
+ * n_timesteps: host int, written; vidx, aidx: host i32 [steps]. */
+h3_status h3_sampler_plan(int steps, float shift_video, float shift_audio, float* timesteps, int* n_timesteps,
+                          int32_t* vidx, int32_t* aidx);
+
 /* One denoiser transition of the sampler over the packed sequence [text | cond | audio | video]:
  *   x[text rows]  = text_x (the projected conditioner rows, computed once by the caller)
  *   x[cond rows]  = embed(z_cond; patch_v),  x[audio rows] = embed(z_audio; patch_a),

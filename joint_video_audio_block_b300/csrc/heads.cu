@@ -20,7 +20,10 @@
 //                  exponential solver of Zhang, Song and Chen, 2023): with the data prediction
 //                  D = z - sigma v, z <- a z + c_now D + c_prev D_prev, D_prev <- D, the weights
 //                  from h3_res_multistep_step.
+#include <algorithm>
 #include <cmath>
+#include <functional>
+#include <vector>
 
 #include "../../include/h3.h"
 #include "kernels.h"
@@ -342,5 +345,38 @@ extern "C" h3_status h3_sigma_schedule(int steps, float shift, float* sigma_out)
                              : std::fma(-step, static_cast<float>(n - 1 - i), end);
     sigma_out[i] = shift * s / (1.f + (shift - 1.f) * s);
   }
+  return H3_OK;
+}
+
+// The plan of a run: both schedules' grids (h3_sigma_schedule), the distinct timesteps 1000 sigma
+// (float32) their transitions evaluate, in descending order -- the rows of the modulation
+// tables -- and each transition's row for video and for audio.  Exact equality decides
+// "distinct": the table must hold the very values the sampler evaluates.
+extern "C" h3_status h3_sampler_plan(int steps, float shift_video, float shift_audio, float* timesteps,
+                                     int* n_timesteps, int32_t* vidx, int32_t* aidx) {
+  if (steps < 1 || !timesteps || !n_timesteps || !vidx || !aidx) return H3_EINVAL;
+  std::vector<float> sv(steps + 1), sa(steps + 1);
+  h3_status st = h3_sigma_schedule(steps, shift_video, sv.data());
+  if (st != H3_OK) return st;
+  if ((st = h3_sigma_schedule(steps, shift_audio, sa.data())) != H3_OK) return st;
+  std::vector<float> tv(steps), ta(steps), all;
+  all.reserve(2 * steps);
+  for (int i = 0; i < steps; ++i) {
+    tv[i] = 1000.f * sv[i];
+    ta[i] = 1000.f * sa[i];
+    all.push_back(tv[i]);
+    all.push_back(ta[i]);
+  }
+  std::sort(all.begin(), all.end(), std::greater<float>());
+  all.erase(std::unique(all.begin(), all.end()), all.end());
+  auto row = [&](float t) {
+    return static_cast<int32_t>(std::lower_bound(all.begin(), all.end(), t, std::greater<float>()) - all.begin());
+  };
+  for (int i = 0; i < steps; ++i) {
+    vidx[i] = row(tv[i]);
+    aidx[i] = row(ta[i]);
+  }
+  std::copy(all.begin(), all.end(), timesteps);
+  *n_timesteps = static_cast<int>(all.size());
   return H3_OK;
 }

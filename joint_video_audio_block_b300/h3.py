@@ -26,7 +26,7 @@ EXPORTS = (
     "h3_status_str", "h3_kernel_timer_start", "h3_kernel_timer_read", "h3_qkv_project",
     "h3_qkv_project_workspace_size", "h3_diag_expire_wait", "h3_attention_sparse", "h3_embed_rows",
     "h3_final_modcache_build", "h3_head_forward", "h3_sigma_schedule", "h3_denoise_step",
-    "h3_res_multistep_step", "h3_head_forward_ms", "h3_denoise_step_ms",
+    "h3_res_multistep_step", "h3_head_forward_ms", "h3_denoise_step_ms", "h3_sampler_plan",
 )
 
 # largest n_rows * head_dim / 2 that h3_qknorm_rope_static's fixed scratch array holds
@@ -99,6 +99,8 @@ def lib():
             "h3_denoise_step": (i32, [D, BW, i32, vp, vp, i32, ctypes.POINTER(h3_io_w), vp, vp, vp, vp, vp, vp, vp, vp,
                                       ctypes.c_float, ctypes.c_float, vp, sz, u32, vp]),
             "h3_res_multistep_step": (i32, [ctypes.c_float, ctypes.c_float, ctypes.c_float, MS]),
+            "h3_sampler_plan": (i32, [i32, ctypes.c_float, ctypes.c_float, ctypes.POINTER(ctypes.c_float),
+                                      ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "h3_head_forward_ms": (i32, [D, vp, i32, vp, vp, vp, i64, vp, vp, i32, MS, vp, vp, vp, vp]),
             "h3_denoise_step_ms": (i32, [D, BW, i32, vp, vp, i32, ctypes.POINTER(h3_io_w), vp, vp, vp, vp, vp, vp, vp,
                                          vp, vp, vp, MS, MS, vp, sz, u32, vp]),
@@ -237,6 +239,16 @@ def h3_denoise_step(dims, blocks, n_blocks, table, table_f, T, io, text_x, z_con
     _check(lib().h3_denoise_step(ctypes.byref(dims), arr, n_blocks, table, table_f, T, ctypes.byref(io), text_x, z_cond,
                                  z_video, z_audio, x, tag, tidx, pos, dsigma_video, dsigma_audio, workspace, ws_bytes,
                                  flags, stream), "h3_denoise_step")
+
+
+def h3_sampler_plan(steps: int, shift_video: float, shift_audio: float):
+    """Host-side run plan: (distinct timesteps descending, video row per step, audio row per step)."""
+    ts = (ctypes.c_float * (2 * steps))()
+    n = ctypes.c_int()
+    vi = (ctypes.c_int * steps)()
+    ai = (ctypes.c_int * steps)()
+    _check(lib().h3_sampler_plan(steps, shift_video, shift_audio, ts, ctypes.byref(n), vi, ai), "h3_sampler_plan")
+    return [ts[i] for i in range(n.value)], list(vi), list(ai)
 
 
 def h3_res_multistep_step(sigma_prev, sigma, sigma_next) -> h3_ms_step:

@@ -62,16 +62,12 @@ def workspace(dims: _h3.h3_dims, n_rows: int, device="cuda") -> torch.Tensor:
 def sampler_plan(steps: int, video_shift: float = 12.0, audio_shift: float = 3.0):
     """Host-side plan of a run: the video and audio sampling grids (h3_sigma_schedule), the
     distinct timesteps (1000 sigma, float32) of the transitions in descending order -- the rows
-    of the modulation tables -- and, per transition, the table row of each schedule."""
+    of the modulation tables -- and, per transition, the table row of each schedule
+    (h3_sampler_plan)."""
     sv = np.asarray(_h3.h3_sigma_schedule(steps, video_shift), np.float32)
     sa = np.asarray(_h3.h3_sigma_schedule(steps, audio_shift), np.float32)
-    tv = np.float32(1000.0) * sv[:steps]
-    ta = np.float32(1000.0) * sa[:steps]
-    values = np.array(sorted(set(tv.tolist()) | set(ta.tolist()), reverse=True), np.float32)
-    index = {float(v): i for i, v in enumerate(values)}
-    vidx = [index[float(v)] for v in tv]
-    aidx = [index[float(v)] for v in ta]
-    return values, sv, sa, vidx, aidx
+    values, vidx, aidx = _h3.h3_sampler_plan(steps, video_shift, audio_shift)
+    return np.asarray(values, np.float32), sv, sa, vidx, aidx
 
 
 def step_tidx(tidx: torch.Tensor, audio_rows: slice, vidx: int, aidx: int) -> torch.Tensor:

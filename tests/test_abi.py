@@ -322,3 +322,32 @@ def test_misaligned_int32_and_float32_arrays_refused(h3mod):
     assert L.h3_denoise_step_ms(ctypes.byref(d), arr, 1, al, al, 1, ctypes.byref(io), al, None, al, al, odd, al, al,
                                 al, al, al, ctypes.byref(step), ctypes.byref(step), ws, big, 0,
                                 None) == h3mod.H3_EINVAL
+
+
+def test_sampler_plan_is_the_oracle_grids_deduplicated(h3mod):
+    """Host-only entry point: the run plan's table rows are the distinct float32 values
+    1000 sigma of both schedules' first `steps` grid points (the oracle's shifted_sigmas),
+    descending, and each transition's rows point at its own values; a 40-step run has 78 rows
+    in float32 (the 12/13 pair of the two grids differs by one ulp; exact arithmetic gives the
+    pages' 77, pinned in the oracle tests)."""
+    import numpy as np
+
+    import oracle.h3_oracle as O
+
+    for steps in (1, 2, 8, 20, 40):
+        tv = np.float32(1000.0) * O.shifted_sigmas(steps, 12.0)[:steps]
+        ta = np.float32(1000.0) * O.shifted_sigmas(steps, 3.0)[:steps]
+        want = sorted(set(tv.tolist()) | set(ta.tolist()), reverse=True)
+        vals, vi, ai = h3mod.h3_sampler_plan(steps, 12.0, 3.0)
+        assert vals == want
+        assert [vals[i] for i in vi] == tv.tolist() and [vals[i] for i in ai] == ta.tolist()
+    assert len(h3mod.h3_sampler_plan(40, 12.0, 3.0)[0]) == 78
+    assert len(h3mod.h3_sampler_plan(8, 12.0, 3.0)[0]) == 15
+    L = h3mod.lib()
+    buf = (ctypes.c_float * 8)()
+    n = ctypes.c_int()
+    idx = (ctypes.c_int * 4)()
+    f = ctypes.c_float
+    assert L.h3_sampler_plan(0, f(12.0), f(3.0), buf, ctypes.byref(n), idx, idx) == h3mod.H3_EINVAL
+    assert L.h3_sampler_plan(4, f(12.0), f(0.0), buf, ctypes.byref(n), idx, idx) == h3mod.H3_EINVAL
+    assert L.h3_sampler_plan(4, f(12.0), f(3.0), None, ctypes.byref(n), idx, idx) == h3mod.H3_EINVAL

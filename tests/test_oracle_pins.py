@@ -800,3 +800,22 @@ def test_denoise_step_multistep_uses_each_modality_s_own_grid():
         want_d = z - sig[1] * v
         np.testing.assert_allclose(dn, want_d, rtol=0, atol=1e-12)
         np.testing.assert_allclose(z2, a * z + cn * want_d + cp * dp, rtol=0, atol=1e-11)
+
+
+def test_two_shifted_grids_give_the_pages_distinct_timestep_counts():
+    """The pages count 77 distinct timesteps for a 40-step run ("AdaLN precompute") and
+    8 + 8 - 1 = 15 for 8 forwards ("Full-resolution 15 s generation").  The reading -- each
+    schedule's first `steps` points of the even grid from 1 to 0, shifted by
+    s sigma / (1 + (s - 1) sigma) with s = 12 (video) and 3 (audio) -- reproduces both in exact
+    rational arithmetic: the grids meet at sigma' = 1, 12/13 and 3/4 for 40 steps, only at 1
+    for 8."""
+    from fractions import Fraction as Fr
+
+    def grid(steps, s):
+        return [Fr(s) * x / (1 + (Fr(s) - 1) * x) for x in (1 - Fr(i, steps) for i in range(steps))]
+
+    for name, steps in (("cache_mb_40_step_run", 40), ("cache_mb_15s_run", 8)):
+        v, a = grid(steps, 12), grid(steps, 3)
+        assert len(set(v) | set(a)) == _page(name)["timesteps"]
+    v, a = set(grid(40, 12)), set(grid(40, 3))
+    assert v & a == {Fr(1), Fr(12, 13), Fr(3, 4)}
