@@ -171,7 +171,7 @@ typedef struct {
  * sigma), sigma_prev being the previous step's sigma (> sigma), or <= 0 for the first step,
  * which is then first order (c_prev = 0; the Euler step).  A step to sigma_next = 0 returns D
  * (a = 0, c_now = 1).  Computed in double precision, rounded once to float.  Anything else
- * returns H3_EINVAL. */
+ * (a NaN anywhere included) returns H3_EINVAL. */
 h3_status h3_res_multistep_step(float sigma_prev, float sigma, float sigma_next, h3_ms_step* out);
 
 /* h3_head_forward with a res_multistep update instead of the Euler one: v as there, then per

@@ -296,7 +296,8 @@ extern "C" h3_status h3_head_forward_ms(const h3_dims* dims, const void* x_rows,
 // takes D constant: a = sigma_next / sigma, c_now = 1 - a (the Euler step); a step to 0
 // returns D (a = 0, c_now = 1).
 extern "C" h3_status h3_res_multistep_step(float sigma_prev, float sigma, float sigma_next, h3_ms_step* out) {
-  if (!out || !(sigma > 0.f) || !(sigma_next >= 0.f) || !(sigma_next < sigma)) return H3_EINVAL;
+  if (!out || !(sigma > 0.f) || !(sigma_next >= 0.f) || !(sigma_next < sigma) || std::isnan(sigma_prev))
+    return H3_EINVAL;
   const bool first = !(sigma_prev > 0.f);
   if (!first && !(sigma_prev > sigma)) return H3_EINVAL;
   const double s = sigma, sn = sigma_next, sp = sigma_prev;

@@ -245,7 +245,9 @@ def test_res_multistep_arguments_refused(h3mod):
     L = h3mod.lib()
     out = h3mod.h3_ms_step()
     f = ctypes.c_float
-    bad = ((0.9, 0.0, 0.0), (0.9, 0.5, 0.5), (0.9, 0.5, 0.6), (0.9, 0.5, -0.1), (0.4, 0.5, 0.25))
+    nan = float("nan")
+    bad = ((0.9, 0.0, 0.0), (0.9, 0.5, 0.5), (0.9, 0.5, 0.6), (0.9, 0.5, -0.1), (0.4, 0.5, 0.25),
+           (nan, 0.5, 0.25), (0.9, nan, 0.25), (0.9, 0.5, nan))
     for sp, s, sn in bad:
         assert L.h3_res_multistep_step(f(sp), f(s), f(sn), ctypes.byref(out)) == h3mod.H3_EINVAL, (sp, s, sn)
     assert L.h3_res_multistep_step(f(-1.0), f(0.5), f(0.25), None) == h3mod.H3_EINVAL
