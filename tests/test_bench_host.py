@@ -113,3 +113,19 @@ def test_reference_arm_line(capsys):
     # other ranks print nothing
     bench.run_reference(args, synth.CONFIGS["tiny"], 1)
     assert capsys.readouterr().out == ""
+
+
+def test_page_canvas_matches_the_pages_figure():
+    """The context measurement's workload and the pages' figure it sits next to come from the
+    pages' 'Performance' table: 37,966 packed rows, 8.8 min per denoising step."""
+    import json
+    import os
+
+    import synth
+
+    fig = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_figures.json")))
+    fig = fig["m3_ultra_step_37966_rows"]
+    assert synth.CONFIGS["trunk37966"].layout.n_rows == fig["rows"]
+    assert bench.PAGES_M3_ULTRA_STEP_S == fig["minutes_per_step"] * 60
+    # one block timed and multiplied by 50 (the page's own extrapolation, within its rounding)
+    assert abs(fig["seconds_per_block"] * 50 / 60 - fig["minutes_per_step"]) <= 0.05 + 1e-9  # 8.75 printed as 8.8
